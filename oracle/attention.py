@@ -1,0 +1,236 @@
+"""fp64 CPU oracle for exact attention: forward (O, LSE) and the explicit-gradient backward.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this module; only the tests,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may call it.  It shares
+no code, constant or helper with the CUDA library.
+
+What it computes, and where the pages fix it:
+
+* Attention is ``softmax(QK^T / sqrt(d)) V`` (FlashAttention page 3, opening formula).  The
+  method "computes the same function as standard attention" (page 2, "Why the word 'exact' is
+  in the title"), so the oracle is that standard function, materialised: S = scale*Q K^T,
+  P = softmax(S) row by row, O = P V (page 3, "前序瓶颈" three-line listing).  ``scale`` is an
+  argument (page 1's pseudocode has none, page 3 uses 1/sqrt(d)).
+* Masks (page 3, list after the CPU reference: causal / padding masks "for production
+  semantics"; page 1, block-sparse paragraph: a tile mask says which blocks are computed).
+  Entry (i, j) of one (b, h) slice is allowed iff
+  ``(not causal or j <= i) and j < kv_len[b] and block_mask[i // 128][j // 128] != 0``.
+  Disallowed scores are -inf.  A row with no allowed key has O = 0 and LSE = -inf (the pages
+  only ask that fully masked rows be covered, page 3 "数值与正确性").
+* Statistics kept for the backward: page 1 (backward paragraph) keeps two length-N vectors
+  (running max and normaliser).  The oracle returns the one equivalent vector
+  ``LSE_i = ln sum_j exp(s_ij)`` (natural log), computed stably as ``m_i + ln sum exp(s_ij - m_i)``.
+* Backward: the pages say only that P is recomputed from the stored statistics (page 1,
+  backward paragraph; page 2, "Tiling, and paying arithmetic to avoid memory").  The gradients
+  of O = softmax(S) V with S = scale*Q K^T follow from the chain rule:
+  dV = P^T dO;  dP = dO V^T;  D_i = sum_j P_ij dP_ij;  dS = P * (dP - D);
+  dQ = scale * dS K;  dK = scale * dS^T Q.
+  The oracle forms D from P and dP (its definition); the CUDA path uses rowsum(dO * O), equal
+  in exact arithmetic.
+* ``online_attention`` and ``merge_stats`` restate the pages' own blockwise algorithm (page 1,
+  tiling and online softmax with a running max and running sum; page 3, "Online softmax" and the
+  (m, l, u) merge law) so that the dense oracle can be checked against the pages' claim that the
+  two agree (page 3, "CPU reference": error below 1e-12 on its worked example).
+
+Large inputs are processed a chunk of query rows at a time (a memory bound only: each chunk
+still forms its full score rows).  When a tile mask removes most columns, a chunk gathers
+the columns that any of its rows may attend to; every other column is masked for the whole
+chunk, contributes exp(-inf) = 0, and leaving it out changes no result.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+TILE = 128          # block-mask granularity (score tiles of 128 x 128)
+ROW_CHUNK = 1024    # query rows per chunk (bounds the size of one score block)
+
+
+def _as_i64_list(x, B: int) -> list:
+    if x is None:
+        return [None] * B
+    return [int(v) for v in np.asarray(x).reshape(-1)]
+
+
+def allowed(rows: np.ndarray, cols: np.ndarray, causal: bool, kv_len: Optional[int],
+            block_mask: Optional[np.ndarray]) -> np.ndarray:
+    """Boolean [len(rows), len(cols)]: which (query, key) pairs enter the softmax."""
+    ok = np.ones((rows.size, cols.size), dtype=bool)
+    if causal:
+        ok &= cols[None, :] <= rows[:, None]
+    if kv_len is not None:
+        ok &= (cols < kv_len)[None, :]
+    if block_mask is not None:
+        bm = np.asarray(block_mask) != 0
+        ok &= bm[(rows // TILE)[:, None], (cols // TILE)[None, :]]
+    return ok
+
+
+def _chunk_cols(rows: np.ndarray, N: int, causal: bool, kv_len, block_mask) -> np.ndarray:
+    """Columns any row of the chunk may attend to (all N when nothing restricts them)."""
+    if block_mask is None and kv_len is None and not causal:
+        return np.arange(N)
+    cols = np.arange(N)
+    ok = allowed(rows, cols, causal, kv_len, block_mask)
+    keep = ok.any(axis=0)
+    return cols[keep]
+
+
+def _scores(q_rows: np.ndarray, k_cols: np.ndarray, scale: float, ok: np.ndarray) -> np.ndarray:
+    s = scale * (q_rows @ k_cols.T)
+    return np.where(ok, s, -np.inf)
+
+
+def _row_lse(s: np.ndarray) -> np.ndarray:
+    """ln sum_j exp(s_ij) per row; -inf for rows with no finite entry."""
+    m = s.max(axis=1) if s.shape[1] else np.full(s.shape[0], -np.inf)
+    finite = np.isfinite(m)
+    m0 = np.where(finite, m, 0.0)
+    with np.errstate(divide="ignore"):
+        lse = m0 + np.log(np.exp(s - m0[:, None]).sum(axis=1)) if s.shape[1] else np.full(s.shape[0], -np.inf)
+    return np.where(finite, lse, -np.inf)
+
+
+def _probs(s: np.ndarray, lse: np.ndarray) -> np.ndarray:
+    finite = np.isfinite(lse)
+    p = np.exp(s - np.where(finite, lse, 0.0)[:, None])
+    p[~finite, :] = 0.0
+    return p
+
+
+def forward(q, k, v, scale: float, causal: bool = False, kv_lens=None, block_mask=None,
+            rows: Optional[Sequence[int]] = None, heads: Optional[Sequence[int]] = None):
+    """Dense masked attention in fp64.
+
+    q, k, v: float64 arrays [B, H, N, d] (k and v may have a different N only when neither
+    causal nor a block mask is set).  Returns (O [B,H,R,d], LSE [B,H,R]) for the R query rows
+    in ``rows`` (default: all rows) and the heads in ``heads`` (default: all heads).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    rows = np.arange(Nq) if rows is None else np.asarray(rows, dtype=np.int64)
+    heads = list(range(H)) if heads is None else list(heads)
+    lens = _as_i64_list(kv_lens, B)
+    O = np.zeros((B, len(heads), rows.size, v.shape[3]))
+    L = np.full((B, len(heads), rows.size), -np.inf)
+    for b in range(B):
+        for hi, h in enumerate(heads):
+            for c0 in range(0, rows.size, ROW_CHUNK):
+                r = rows[c0:c0 + ROW_CHUNK]
+                cols = _chunk_cols(r, Nk, causal, lens[b], block_mask)
+                ok = allowed(r, cols, causal, lens[b], block_mask)
+                s = _scores(q[b, h, r], k[b, h, cols], scale, ok)
+                lse = _row_lse(s)
+                p = _probs(s, lse)
+                O[b, hi, c0:c0 + r.size] = p @ v[b, h, cols]
+                L[b, hi, c0:c0 + r.size] = lse
+    return O, L
+
+
+def probabilities(q, k, scale: float, causal: bool = False, kv_len=None, block_mask=None):
+    """P = softmax(S) for one (b, h) slice: q [Nq, d], k [Nk, d] -> [Nq, Nk] (rows sum to 1)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    rows, cols = np.arange(q.shape[0]), np.arange(k.shape[0])
+    s = _scores(q, k, scale, allowed(rows, cols, causal, kv_len, block_mask))
+    return _probs(s, _row_lse(s))
+
+
+def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, block_mask=None,
+             heads: Optional[Sequence[int]] = None, return_delta: bool = False):
+    """Explicit-gradient backward of dense masked attention, fp64.
+
+    Returns (dQ, dK, dV), each [B, len(heads), N, d]; with ``return_delta`` also D [B,H',N]
+    where D_i = sum_j P_ij dP_ij.  Rows whose LSE is -inf contribute nothing.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    B, H, N, d = q.shape
+    heads = list(range(H)) if heads is None else list(heads)
+    lens = _as_i64_list(kv_lens, B)
+    dQ = np.zeros((B, len(heads), N, d))
+    dK = np.zeros((B, len(heads), k.shape[2], d))
+    dV = np.zeros((B, len(heads), v.shape[2], v.shape[3]))
+    Dd = np.zeros((B, len(heads), N))
+    for b in range(B):
+        for hi, h in enumerate(heads):
+            for c0 in range(0, N, ROW_CHUNK):
+                r = np.arange(c0, min(N, c0 + ROW_CHUNK))
+                cols = _chunk_cols(r, k.shape[2], causal, lens[b], block_mask)
+                ok = allowed(r, cols, causal, lens[b], block_mask)
+                s = _scores(q[b, h, r], k[b, h, cols], scale, ok)
+                p = _probs(s, _row_lse(s))
+                dp = do[b, h, r] @ v[b, h, cols].T
+                D = (p * dp).sum(axis=1)
+                ds = p * (dp - D[:, None])
+                dQ[b, hi, r] = scale * (ds @ k[b, h, cols])
+                dK[b, hi, cols] += scale * (ds.T @ q[b, h, r])
+                dV[b, hi, cols] += p.T @ do[b, h, r]
+                Dd[b, hi, r] = D
+    if return_delta:
+        return dQ, dK, dV, Dd
+    return dQ, dK, dV
+
+
+# --- the pages' own blockwise algorithm, for pinning the dense oracle -----------------------
+
+def stats(scores: np.ndarray, values: np.ndarray):
+    """(m, l, u) of one group of scores for one query (page 3, "Online softmax" statistics).
+
+    m = max_i s_i, l = sum_i exp(s_i - m), u = sum_i exp(s_i - m) v_i.  An empty or fully
+    masked group is the identity (-inf, 0, 0).
+    """
+    scores = np.asarray(scores, dtype=np.float64)
+    values = np.asarray(values, dtype=np.float64)
+    if scores.size == 0 or not np.isfinite(scores).any():
+        return -math.inf, 0.0, np.zeros(values.shape[-1])
+    m = float(scores.max())
+    w = np.exp(scores - m)
+    return m, float(w.sum()), w @ values
+
+
+def merge_stats(a, b):
+    """Stable merge of two (m, l, u) triples (page 3, merge law under "Online softmax")."""
+    ma, la, ua = a
+    mb, lb, ub = b
+    m = max(ma, mb)
+    if m == -math.inf:
+        return -math.inf, 0.0, np.zeros_like(np.asarray(ua, dtype=np.float64))
+    fa = math.exp(ma - m) if ma != -math.inf else 0.0
+    fb = math.exp(mb - m) if mb != -math.inf else 0.0
+    return m, fa * la + fb * lb, fa * np.asarray(ua) + fb * np.asarray(ub)
+
+
+def online_attention(q, k, v, scale: float, block_size: int):
+    """Blockwise attention with a running max and running normaliser (no masks).
+
+    For one (b, h) slice: q [Nq, d], k [Nk, d], v [Nk, dv].  Keys and values are visited one
+    block at a time; each query keeps its running maximum, normaliser and un-normalised output,
+    rescaling the old contributions by exp(m_old - m_new) whenever the maximum grows, and
+    divides by the normaliser at the end (page 1, tiling and online softmax; page 3, CPU
+    reference).  Returns (O [Nq, dv], LSE [Nq]).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    nq = q.shape[0]
+    run_max = np.full(nq, -np.inf)
+    run_sum = np.zeros(nq)
+    acc = np.zeros((nq, v.shape[1]))
+    for start in range(0, k.shape[0], block_size):
+        kb, vb = k[start:start + block_size], v[start:start + block_size]
+        s = scale * (q @ kb.T)
+        new_max = np.maximum(run_max, s.max(axis=1))
+        shrink = np.exp(run_max - new_max)          # exp(-inf) = 0 on the first block
+        w = np.exp(s - new_max[:, None])
+        run_sum = shrink * run_sum + w.sum(axis=1)
+        acc = shrink[:, None] * acc + w @ vb
+        run_max = new_max
+    return acc / run_sum[:, None], run_max + np.log(run_sum)

@@ -1,0 +1,63 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check that the pins in
+test_oracle.py catch every one: a dropped scale, a sign, a transposed operand, an off-by-one in
+each mask, the wrong logarithm base, a wrong reduction axis, a wrong rescale direction in the
+pages' online algorithm and a wrong factor in the pages' merge law."""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = [
+    ("dQ[b, hi, r] = scale * (ds @ k[b, h, cols])", "dQ[b, hi, r] = (ds @ k[b, h, cols])"),
+    ("ds = p * (dp - D[:, None])", "ds = p * (dp + D[:, None])"),
+    ("dK[b, hi, cols] += scale * (ds.T @ q[b, h, r])", "dK[b, hi, cols] += scale * (ds @ q[b, h, r])"),
+    ("dV[b, hi, cols] += p.T @ do[b, h, r]", "dV[b, hi, cols] += p.T @ do[b, h, r] * 1.0001"),
+    ("ok &= cols[None, :] <= rows[:, None]", "ok &= cols[None, :] < rows[:, None]"),
+    ("ok &= (cols < kv_len)[None, :]", "ok &= (cols <= kv_len)[None, :]"),
+    ("ok &= bm[(rows // TILE)[:, None], (cols // TILE)[None, :]]",
+     "ok &= bm[(cols // TILE)[None, :], (rows // TILE)[:, None]]"),
+    ("s = scale * (q_rows @ k_cols.T)", "s = (q_rows @ k_cols.T)"),
+    ("lse = m0 + np.log(np.exp(s - m0[:, None]).sum(axis=1))",
+     "lse = m0 + np.log2(np.exp(s - m0[:, None]).sum(axis=1))"),
+    ("O[b, hi, c0:c0 + r.size] = p @ v[b, h, cols]", "O[b, hi, c0:c0 + r.size] = p @ v[b, h, cols[::-1]]"),
+    ("shrink = np.exp(run_max - new_max)", "shrink = np.exp(new_max - run_max)"),
+    ("return m, fa * la + fb * lb, fa * np.asarray(ua) + fb * np.asarray(ub)",
+     "return m, fa * la + fb * lb, fa * np.asarray(ua) + fa * np.asarray(ub)"),
+]
+
+
+@pytest.fixture(scope="module")
+def sandbox(tmp_path_factory):
+    d = tmp_path_factory.mktemp("mut")
+    for name in ("oracle", "workloads"):
+        shutil.copytree(os.path.join(ROOT, name), d / name,
+                        ignore=shutil.ignore_patterns("__pycache__"))
+    (d / "tests").mkdir()
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), d / "tests" / "golden")
+    for f in ("conftest.py", "test_oracle.py"):
+        shutil.copy(os.path.join(ROOT, "tests", f), d / "tests" / f)
+    return d
+
+
+def test_clean_copy_passes(sandbox):
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", "tests/test_oracle.py"],
+                       cwd=sandbox, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout[-2000:]
+
+
+@pytest.mark.parametrize("old,new", MUTATIONS, ids=[m[1][:40] for m in MUTATIONS])
+def test_planted_mistake_is_caught(sandbox, old, new):
+    path = sandbox / "oracle" / "attention.py"
+    src = open(os.path.join(ROOT, "oracle", "attention.py")).read()
+    assert old in src
+    path.write_text(src.replace(old, new))
+    try:
+        r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", "tests/test_oracle.py"],
+                           cwd=sandbox, capture_output=True, text=True)
+        assert r.returncode != 0, f"mutation not caught: {new}"
+    finally:
+        path.write_text(src)

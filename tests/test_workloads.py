@@ -1,0 +1,34 @@
+"""Input recipe checks: seeded determinism, dtype rounding, valid-length range, tile pattern."""
+import torch
+
+from workloads import WORKLOADS, local_global_tile_mask, make_inputs
+
+
+def test_tile_pattern_count_n64k():
+    """512 x 512 tiles, kept iff |I-J| <= 4 or I < 2 or J < 2.
+    Band: 512*9 - 2*(4+3+2+1) = 4588; global rows or columns: 2*512 + 2*512 - 4 = 2044;
+    band tiles inside the global rows/columns: 5+6+5+6-4 = 18; total 4588 + 2044 - 18 = 6614."""
+    bm = local_global_tile_mask(512)
+    assert bm.dtype == torch.uint8 and tuple(bm.shape) == (512, 512)
+    assert int(bm.sum()) == 6614
+    assert bm[0].all() and bm[:, 1].all() and bm[300, 296] == 1 and bm[300, 295] == 0
+
+
+def test_seeded_and_rounded():
+    w = WORKLOADS["bert_large_pad_n512"]
+    a = make_inputs(w, seed=0, heads=2)
+    b = make_inputs(w, seed=0, heads=2)
+    for key in ("q", "k", "v", "do", "kv_lens"):
+        assert torch.equal(a[key], b[key])
+    assert a["q"].dtype == torch.bfloat16
+    lens = a["kv_lens"]
+    assert lens.dtype == torch.int32 and int(lens.min()) >= 256 and int(lens.max()) <= 512
+    c = make_inputs(w, seed=1, heads=2)
+    assert not torch.equal(a["q"], c["q"])
+
+
+def test_value_scale_and_fp32():
+    g = make_inputs(WORKLOADS["gpt2_small_causal_n1024"], heads=1, B=1)
+    assert 1.3 < float(g["q"].float().std()) < 1.7 and g["causal"]
+    f = make_inputs(WORKLOADS["fp32_n128_d64"])
+    assert f["q"].dtype == torch.float32 and tuple(f["q"].shape) == (1, 1, 128, 64)
