@@ -1,0 +1,341 @@
+"""Throughput of exact attention (forward + recompute backward) on GB300, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one pass of the whole path over one batch: fa_forward then fa_backward on the
+workload's synthetic inputs (seeded N(0,1), see workloads/).  The default workload is the
+long-context shape B1 H16 N16384 d128, non-causal, the shape the bf16 tensor-peak target is
+quoted on.  Its inputs (Q, K, V, O, dO: 5 x 64 MiB) are larger than the 129 MB L2, so no flush
+is needed between steps.
+
+FLOP convention: forward F = 4*B*H*N^2*d (halved when causal; kept 128x128 tiles only when
+block-sparse).  The headline value counts 2.5*F per forward+backward step; the algorithmic
+count (2 products forward, 5 backward: 3.5*F) is reported beside it.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (independent replicas,
+weak scaling); the ranks only meet at the barriers around the timed region and for the max of
+the elapsed times.  --impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd & fwd+bwd TFLOPS, % of GB300 BF16 tensor peak, N=512–16K"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["exact_io_aware_23_gb300/csrc"]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for d in KERNEL_SOURCES:
+        base = os.path.join(ROOT, d)
+        for fn in sorted(os.listdir(base)):
+            if fn.endswith((".cu", ".cuh")):
+                with open(os.path.join(base, fn), "rb") as f:
+                    h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def forward_flops(w, B, H, N, block_mask=None):
+    full = 4.0 * B * H * N * N * w.d
+    if block_mask is not None:
+        T = block_mask.shape[0]
+        return full * float(block_mask.sum()) / float(T * T)
+    return full / 2 if w.causal else full
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons every 200 ms while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:8]) if v == "Active"})
+        pw = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max(pw) if pw else None, "samples": len(self.rows)}
+
+
+def cpu_oracle_sample(x, w, rows_per_head, heads=(0,)):
+    """Time the fp64 oracle, forward + backward, on a sample of query rows of some heads."""
+    import numpy as np
+    import torch
+
+    import oracle
+    f64 = lambda t: t[:, list(heads)].to(torch.float64).numpy()
+    qq, kk, vv, dd = (f64(x[n]) for n in ("q", "k", "v", "do"))
+    kv = None if x["kv_lens"] is None else x["kv_lens"].numpy()
+    bm = None if x["block_mask"] is None else x["block_mask"].numpy()
+    rows = np.arange(rows_per_head)
+    t0 = time.perf_counter()
+    oracle.forward(qq, kk, vv, x["scale"], causal=x["causal"], kv_lens=kv, block_mask=bm, rows=rows)
+    oracle.backward(qq, kk, vv, dd, x["scale"], causal=x["causal"], kv_lens=kv, block_mask=bm,
+                    rows=rows)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, w):
+    """The oracle as the reference arm: each step = fwd+bwd on a bounded row sample of one head."""
+    from workloads import make_inputs
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    x = make_inputs(w, seed=0, heads=1, B=1)
+    F1 = forward_flops(w, 1, 1, w.N, x["block_mask"])       # one head
+    rows = args.ref_rows
+    f_sample = 2.5 * F1 * rows / w.N
+    for _ in range(args.warmup):
+        cpu_oracle_sample(x, w, rows)
+    t = sum(cpu_oracle_sample(x, w, rows) for _ in range(args.steps))
+    value = f_sample * args.steps / t / 1e12
+    sample = f"fp64 oracle fwd+bwd on query rows [0,{rows}) of head 0 of {w.name} per step"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "key_padding": w.pad_lengths is not None, "block_sparse": w.block_sparse,
+            "dtype": w.dtype, "parallelism": "replicas",
+            "l2": "inputs larger than L2 (no flush)"}
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import exact_io_aware_23_gb300 as fa
+    from workloads import make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    x = make_inputs(w, seed=rank)
+    B, H, N, d = x["q"].shape
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    bm = None if x["block_mask"] is None else x["block_mask"].to(dev)
+    kl = None if x["kv_lens"] is None else x["kv_lens"].to(dev)
+    o, lse = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.backward_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    kw = dict(causal=w.causal, scale=w.scale, block_mask=bm, kv_lens=kl)
+
+    def step():
+        fa.forward(q, k, v, o=o, lse=lse, **kw)
+        fa.backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.check_device_status() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            fa.forward(q, k, v, o=o, lse=lse, **kw)
+            ev[i][1].record(stream)
+            fa.backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
+            ev[i][2].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    total_ms = start.elapsed_time(end)
+    t_fwd = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    t_bwd = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    if fa.check_device_status() != 0:
+        raise RuntimeError("device error during the timed region")
+
+    # end to end: pinned host inputs -> device, fwd + bwd, results back to pinned host memory
+    hin = [t.pin_memory() for t in (x["q"], x["k"], x["v"], x["do"])]
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+    din = [q, k, v, do]
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def e2e_step():
+        for dst, src in zip(din, hin):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(hout, (o, lse, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    s2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = s2.elapsed_time(e2)
+
+    times = torch.tensor([total_ms, e2e_ms, t_fwd, t_bwd], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms, t_fwd, t_bwd = times.tolist()
+
+    F = forward_flops(w, B, H, N, x["block_mask"])
+    ms_step = total_ms / args.steps
+    value = world * 2.5 * F / (ms_step * 1e-3) / 1e12
+    e2e_value = world * 2.5 * F / (e2e_ms / args.steps * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    fwd_tf = F / (t_fwd * 1e-3) / 1e12
+    bwd_tf = 2.5 * F / (t_bwd * 1e-3) / 1e12
+    dominant = "backward" if t_bwd >= t_fwd else "forward"
+    achieved = bwd_tf if dominant == "backward" else fwd_tf
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        with open(tp) as f:
+            rec = json.load(f)
+        ent = rec.get(w.name, {}).get(dominant)
+        if ent and ent.get("source_hash") == kernel_source_hash():
+            traffic = ent.get("bytes_per_launch")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": workload_config(w),
+        "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+        "fwd_bwd_tflops_algorithmic": world * 3.5 * F / (ms_step * 1e-3) / 1e12,
+        "pct_of_bf16_peak": {"forward": fwd_tf / peak, "fwd_bwd": value / world / peak,
+                             "peak_tflops": peak, "peak_source": peak_src},
+        "ms_fwd": t_fwd, "ms_bwd": t_bwd,
+        "roofline": {"bound": "tensor", "kernel": f"fa_{dominant} (all launches of the call)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"bf16_tflops of {peak_src}"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = min(N, args.cpu_rows)
+        t_cpu = cpu_oracle_sample(x, w, rows)
+        f_cpu = 2.5 * forward_flops(w, 1, 1, N, x["block_mask"]) * rows / N
+        line["cpu_baseline"] = {"value": f_cpu / t_cpu / 1e12, "unit": UNIT, "cores": cpu_cores(),
+                                "kind": "oracle",
+                                "sample": f"fp64 oracle fwd+bwd, head 0, query rows [0,{rows}), "
+                                          f"{t_cpu:.1f} s"}
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# kernels of ours launched per step: forward 1, backward 3 (preprocess, main, dQ convert)
+LAUNCHES_PER_STEP = 4
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long_n16k_d128")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=16384)
+    ap.add_argument("--ref-rows", type=int, default=1024)
+    args = ap.parse_args()
+    from workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+"""Python binding of libfa, the exact-attention C ABI (include/fa.h), for GB300 (sm_103a).
+
+This module only marshals arguments: it checks tensor placement, dtype and shape, passes raw
+device pointers and the current CUDA stream to the C functions, and turns a non-OK status into
+an exception.  Every step of the computation runs in the library's CUDA kernels.  Importing
+fails loudly when the library has not been built (``__graft_entry__.build()``); there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = ["forward", "backward", "backward_workspace_size", "check_device_status",
+           "set_fault_injection", "set_wait_limit_ms", "FaError", "LIB_PATH", "lib"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_BF16, FA_FP32 = 0, 1
+_DTYPES = {torch.bfloat16: FA_BF16, torch.float32: FA_FP32}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {lib.fa_status_string(status).decode()}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libfa.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.fa_forward.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp, vp]
+    L.fa_forward.restype = i
+    L.fa_backward_workspace_size.argtypes = [i, i, i, i]
+    L.fa_backward_workspace_size.restype = sz
+    L.fa_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp,
+                              vp, sz, vp]
+    L.fa_backward.restype = i
+    L.fa_check_device_status.argtypes = [vp]
+    L.fa_check_device_status.restype = i
+    L.fa_status_string.argtypes = [i]
+    L.fa_status_string.restype = ctypes.c_char_p
+    L.fa_debug_set_fault_injection.argtypes = [i]
+    L.fa_debug_set_fault_injection.restype = None
+    L.fa_debug_set_wait_limit_ms.argtypes = [ctypes.c_uint32]
+    L.fa_debug_set_wait_limit_ms.restype = None
+    L.fa_version.argtypes = []
+    L.fa_version.restype = i
+    return L
+
+
+lib = _load()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_qkv(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [B, H, N, d]")
+    if not (q.shape == k.shape == v.shape) or not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share shape and dtype")
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    return q.shape
+
+
+def _masks(block_mask, kv_lens, B, N, device):
+    if block_mask is not None:
+        T = (N + 127) // 128
+        if block_mask.dtype != torch.uint8 or tuple(block_mask.shape) != (T, T):
+            raise ValueError(f"block_mask must be uint8 [{T}, {T}]")
+        block_mask = block_mask.to(device).contiguous()
+    if kv_lens is not None:
+        if kv_lens.dtype != torch.int32 or tuple(kv_lens.shape) != (B,):
+            raise ValueError(f"kv_lens must be int32 [{B}]")
+        kv_lens = kv_lens.to(device).contiguous()
+    return block_mask, kv_lens
+
+
+def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = False,
+            scale: Optional[float] = None, block_mask: Optional[torch.Tensor] = None,
+            kv_lens: Optional[torch.Tensor] = None, o: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """O, LSE = attention forward (fa_forward).  q, k, v: [B, H, N, d] bf16 or fp32 on CUDA."""
+    B, H, N, d = _check_qkv(q, k, v)
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    block_mask, kv_lens = _masks(block_mask, kv_lens, B, N, q.device)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = lib.fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
+                        int(bool(causal)), _ptr(block_mask), _DTYPES[q.dtype], _ptr(kv_lens),
+                        _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_forward")
+    return o, lse
+
+
+def backward_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(lib.fa_backward_workspace_size(B, H, N, d))
+
+
+def backward(q, k, v, o, lse, do, *, causal: bool = False, scale: Optional[float] = None,
+             block_mask=None, kv_lens=None, dq=None, dk=None, dv=None, workspace=None,
+             stream=None):
+    """dQ, dK, dV = recompute-based attention backward (fa_backward)."""
+    B, H, N, d = _check_qkv(q, k, v)
+    for name, t in (("o", o), ("do", do)):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must match q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be fp32 [B, H, N]")
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    block_mask, kv_lens = _masks(block_mask, kv_lens, B, N, q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = backward_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib.fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                         _ptr(dk), _ptr(dv), B, H, N, d, scale, int(bool(causal)),
+                         _ptr(block_mask), _DTYPES[q.dtype], _ptr(kv_lens), _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_backward")
+    return dq, dk, dv
+
+
+def check_device_status(stream=None) -> int:
+    """Synchronise the stream and return the device status (FA_OK or FA_ERR_TIMEOUT/CUDA)."""
+    return int(lib.fa_check_device_status(_stream(stream)))
+
+
+def set_fault_injection(mode: int) -> None:
+    lib.fa_debug_set_fault_injection(int(mode))
+
+
+def set_wait_limit_ms(ms: int) -> None:
+    lib.fa_debug_set_wait_limit_ms(int(ms))

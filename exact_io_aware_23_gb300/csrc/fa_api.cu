@@ -1,0 +1,149 @@
+// C-ABI layer of libfa: argument validation, dispatch to the kernels, the per-device error
+// word and the failure-detection test hooks.  See include/fa.h for the contract.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "fa_internal.cuh"
+
+namespace {
+
+// Per-device error word written by kernels whose bounded waits ran out.
+__device__ int g_fa_error_word;
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices] = {nullptr};
+std::atomic<int> g_inject{0};
+std::atomic<uint32_t> g_wait_limit_ms{2000};
+
+fa_status device_error_word(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_error_word) != cudaSuccess) return FA_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_common(int B, int H, int N, int d, float scale, fa_dtype dtype) {
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (H > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa::DebugKnobs knobs() {
+  fa::DebugKnobs k;
+  k.inject = g_inject.load();
+  k.wait_limit_ms = g_wait_limit_ms.load();
+  return k;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_UNKNOWN_STATUS";
+}
+
+void fa_debug_set_fault_injection(int mode) { g_inject.store(mode); }
+
+void fa_debug_set_wait_limit_ms(uint32_t ms) { g_wait_limit_ms.store(ms == 0 ? 2000u : ms); }
+
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int N, int d, float scale, int causal,
+                     const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                     void* stream) {
+  fa_status st = check_common(B, H, N, d, scale, dtype);
+  if (st != FA_OK) return st;
+  if (B == 0 || H == 0 || N == 0) return FA_OK;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  fa::FwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.B = B; a.H = H; a.N = N; a.d = d; a.scale = scale; a.causal = causal != 0;
+  a.block_mask = block_mask; a.n_tiles = (N + fa::kMaskTile - 1) / fa::kMaskTile;
+  a.kv_lens = kv_lens; a.dbg = knobs();
+  if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_fwd_simt(a, dtype, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_backward_workspace_size(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
+  const size_t rows = (size_t)B * H * N;
+  return round_up(rows * (size_t)d * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+}
+
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
+                      const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                      int B, int H, int N, int d, float scale, int causal,
+                      const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  fa_status st = check_common(B, H, N, d, scale, dtype);
+  if (st != FA_OK) return st;
+  if (B == 0 || H == 0 || N == 0) return FA_OK;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
+  if (workspace_bytes < fa_backward_workspace_size(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  fa::BwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.dO = dO; a.lse = lse; a.dq = dq; a.dk = dk; a.dv = dv;
+  const size_t rows = (size_t)B * H * N;
+  a.dq_acc = static_cast<float*>(workspace);
+  a.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                     round_up(rows * (size_t)d * sizeof(float), 256));
+  a.B = B; a.H = H; a.N = N; a.d = d; a.scale = scale; a.causal = causal != 0;
+  a.block_mask = block_mask; a.n_tiles = (N + fa::kMaskTile - 1) / fa::kMaskTile;
+  a.kv_lens = kv_lens; a.dbg = knobs();
+  if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_bwd_preprocess(a, dtype, s);
+  if (e == cudaSuccess)
+    e = fa::launch_bwd_simt(a, dtype, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_dq_convert(a, dtype, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_check_device_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+  int* p = nullptr;
+  if (device_error_word(&p) != FA_OK) return FA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+}  // extern "C"

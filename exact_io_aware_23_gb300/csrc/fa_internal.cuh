@@ -1,0 +1,69 @@
+// Internal declarations shared by the translation units of libfa: launch parameters and the
+// launchers each kernel file exports to the C-ABI layer (fa_api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+constexpr int kMaskTile = 128;   // granularity of the block-sparse tile mask
+
+// Error word written by kernels (one per device, read by fa_check_device_status).
+enum DeviceError : int { kDevOk = 0, kDevTimeout = 1 };
+
+struct DebugKnobs {
+  int inject;              // 1: skip the first K/V tile load of every CTA (watchdog test)
+  uint32_t wait_limit_ms;  // bound of every mbarrier wait
+};
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, H, N, d;
+  float scale;
+  int causal;
+  const uint8_t* block_mask;  // [T, T] or null
+  int n_tiles;                // T = ceil(N / 128)
+  const int32_t* kv_lens;     // [B] or null
+  int* err;                   // device error word
+  DebugKnobs dbg;
+};
+
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dO;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;    // workspace: fp32 [B, H, N, d]
+  float* delta;     // workspace: fp32 [B, H, N], D_i = rowsum(dO_i * O_i)
+  int B, H, N, d;
+  float scale;
+  int causal;
+  const uint8_t* block_mask;
+  int n_tiles;
+  const int32_t* kv_lens;
+  int* err;
+  DebugKnobs dbg;
+};
+
+// CUDA-core (SIMT) kernels: the fp32 path.
+cudaError_t launch_fwd_simt(const FwdArgs& a, fa_dtype dt, cudaStream_t s);
+cudaError_t launch_bwd_simt(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
+
+// Shared backward pieces: D = rowsum(dO * O) with dQ accumulator zeroing, and the final dQ
+// scale + convert.
+cudaError_t launch_bwd_preprocess(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
+cudaError_t launch_bwd_dq_convert(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
+
+}  // namespace fa

@@ -1,0 +1,130 @@
+/*
+ * fa.h - exact, IO-aware attention (FlashAttention forward and recompute backward) for GB300
+ * (sm_103a).  C ABI: plain pointers and sizes, no C++ or framework types.
+ *
+ * The operation.  For every batch b and head h, with q_i, k_j, v_j the rows of one [N, d]
+ * slice of Q, K, V:
+ *     s_ij = scale * (q_i . k_j)  if allowed(i, j), else -inf
+ *     O_i  = sum_j softmax_j(s_ij) v_j,     LSE_i = ln sum_j exp(s_ij)
+ * ("FlashAttention：让精确注意力服从内存层次", opening formula softmax(QK^T/sqrt(d))V; the method computes the same function as standard attention,
+ * "FlashAttention: Exact Attention with Less GPU Memory", section "Why the word 'exact' is in
+ * the title").  The N x N score and probability matrices are computed tile by tile on chip
+ * with an online softmax and never written to device memory ("FlashAttention paper story",
+ * tiling and online-softmax paragraphs).  The forward keeps one statistic per row, the
+ * log-sum-exp, from which the backward recomputes P ("FlashAttention paper story", backward
+ * paragraph: only the softmax statistics are stored and P is rebuilt on chip).
+ *
+ *     allowed(i, j) = (!causal || j <= i)                      causal mask, top-left aligned
+ *                  && (kv_lens == NULL || j < kv_lens[b])       key padding
+ *                  && (block_mask == NULL ||
+ *                      block_mask[(i / 128) * T + (j / 128)] != 0)   block-sparse tile mask
+ *     with T = ceil(N / 128).  A tile whose mask entry is 0 is skipped: its K/V rows are not
+ *     loaded ("FlashAttention paper story", block-sparse paragraph).
+ *     A query row with no allowed key gets O_i = 0 and LSE_i = -inf; its gradients are 0.
+ *
+ * Layout and ownership (all calls).
+ *   - Q, K, V, O, dO, dQ, dK, dV: contiguous [B, H, N, d] row-major (d innermost), in the
+ *     dtype given; device memory owned by the caller; base addresses 16-byte aligned.
+ *   - LSE: float32 [B, H, N], natural log.  kv_lens: int32 [B].  block_mask: uint8 [T, T],
+ *     row-major, one mask for every (b, h).  All device pointers.
+ *   - d must be 64 or 128.  N >= 1 (B, H or N equal to 0 is a no-op returning FA_OK).
+ *   - The library allocates no device memory.  The backward's scratch (fp32 dQ accumulator
+ *     and the per-row D = rowsum(dO * O)) is the caller's workspace.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).  A
+ *     return of FA_OK means the kernels were launched.  Argument errors are detected on the
+ *     host before anything is launched.  No call aborts or throws.
+ *   - Device-side failures (a bounded wait that ran out inside a kernel) are recorded in a
+ *     per-device error word and reported by fa_check_device_status().
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer, bad scale */
+  FA_ERR_UNSUPPORTED = 2,   /* head dim other than 64/128, unknown dtype, size limits */
+  FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or a launch failed */
+  FA_ERR_TIMEOUT = 4        /* a kernel's bounded wait ran out (see fa_check_device_status) */
+} fa_status;
+
+typedef enum {
+  FA_BF16 = 0,              /* bf16 inputs and outputs, fp32 accumulation (tcgen05 path) */
+  FA_FP32 = 1               /* fp32 inputs and outputs, fp32 CUDA-core arithmetic */
+} fa_dtype;
+
+/*
+ * Forward pass.  Writes O [B,H,N,d] (dtype) and LSE [B,H,N] (fp32).
+ *   q, k, v    : inputs, [B,H,N,d] in `dtype`
+ *   o          : output, [B,H,N,d] in `dtype` (must not alias q/k/v)
+ *   lse        : output, [B,H,N] fp32, ln of the softmax normaliser of each query row
+ *   scale      : multiplies q.k before the softmax (1/sqrt(d) for standard attention); finite
+ *   causal     : nonzero = mask keys j > i
+ *   block_mask : nullable; [T,T] uint8 tile mask (0 = tile skipped)
+ *   kv_lens    : nullable; [B] int32 valid key count per sequence (keys j >= kv_lens[b]
+ *                are masked for every query; values are clamped to [0, N])
+ *   stream     : cudaStream_t to launch on
+ */
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int N, int d, float scale, int causal,
+                     const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                     void* stream);
+
+/* Bytes of workspace fa_backward needs for these sizes (a multiple of 256). */
+size_t fa_backward_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Recompute-based backward.  Given the forward's inputs, its O and LSE, and dO, writes
+ * dQ, dK, dV ([B,H,N,d], dtype).  P is rebuilt from LSE tile by tile; the N x N matrices are
+ * never stored ("FlashAttention paper story", backward paragraph).  Gradients:
+ *     dV = P^T dO,  dP = dO V^T,  D_i = rowsum(dO_i * O_i),  dS = P * (dP - D),
+ *     dQ = scale * dS K,  dK = scale * dS^T Q.
+ *   o, lse      : the forward's outputs for the same inputs and mask settings
+ *   dO          : incoming gradient of O
+ *   dq, dk, dv  : outputs (must not alias any input)
+ *   workspace   : device scratch of at least fa_backward_workspace_size(B,H,N,d) bytes,
+ *                 256-byte aligned, owned by the caller; its contents on entry do not matter
+ *                 and are overwritten.  Two calls in flight at once need two workspaces.
+ * Other arguments as in fa_forward.  The result of concurrent dQ accumulation is
+ * nondeterministic in the last bits (fp32 atomic add order).
+ */
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
+                      const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                      int B, int H, int N, int d, float scale, int causal,
+                      const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error word.  Returns
+ * FA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last check, FA_ERR_CUDA if
+ * the synchronisation reported a CUDA error, FA_OK otherwise.
+ */
+fa_status fa_check_device_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Test hooks for the failure-detection path (no fault is involved).  mode 1 makes the next
+ * launches of the tensor-core forward skip issuing their first K/V tile load, so the
+ * consumers' bounded waits run out; the kernel then records FA_ERR_TIMEOUT and returns
+ * normally.  wait_limit_ms sets the bound of every such wait (default 2000 ms; 0 restores it).
+ * Both settings are process-wide.
+ */
+void fa_debug_set_fault_injection(int mode);
+void fa_debug_set_wait_limit_ms(uint32_t wait_limit_ms);
+
+/* ABI version of this header: major * 100 + minor. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -142,11 +142,14 @@ def probabilities(q, k, scale: float, causal: bool = False, kv_len=None, block_m
 
 
 def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, block_mask=None,
-             heads: Optional[Sequence[int]] = None, return_delta: bool = False):
+             heads: Optional[Sequence[int]] = None, return_delta: bool = False,
+             rows: Optional[Sequence[int]] = None):
     """Explicit-gradient backward of dense masked attention, fp64.
 
     Returns (dQ, dK, dV), each [B, len(heads), N, d]; with ``return_delta`` also D [B,H',N]
-    where D_i = sum_j P_ij dP_ij.  Rows whose LSE is -inf contribute nothing.
+    where D_i = sum_j P_ij dP_ij.  Rows whose LSE is -inf contribute nothing.  ``rows``
+    restricts the computation to those query rows: dQ and D are filled for them only and dK,
+    dV hold only their contributions (a sample of the work, used for timing).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -159,10 +162,11 @@ def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, bloc
     dK = np.zeros((B, len(heads), k.shape[2], d))
     dV = np.zeros((B, len(heads), v.shape[2], v.shape[3]))
     Dd = np.zeros((B, len(heads), N))
+    all_rows = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
     for b in range(B):
         for hi, h in enumerate(heads):
-            for c0 in range(0, N, ROW_CHUNK):
-                r = np.arange(c0, min(N, c0 + ROW_CHUNK))
+            for c0 in range(0, all_rows.size, ROW_CHUNK):
+                r = all_rows[c0:c0 + ROW_CHUNK]
                 cols = _chunk_cols(r, k.shape[2], causal, lens[b], block_mask)
                 ok = allowed(r, cols, causal, lens[b], block_mask)
                 s = _scores(q[b, h, r], k[b, h, cols], scale, ok)

@@ -1,0 +1,101 @@
+"""The C-ABI library loads and exports every function include/fa.h declares, and its host-side
+argument checks return the documented status before any CUDA call (CPU only: no kernel runs)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+LIB = os.path.join(ROOT, "exact_io_aware_23_gb300", "libfa.so")
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        import __graft_entry__
+        __graft_entry__.build()
+    L = ctypes.CDLL(LIB)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.fa_forward.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp, vp]
+    L.fa_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp, vp, sz, vp]
+    L.fa_backward_workspace_size.argtypes = [i, i, i, i]
+    L.fa_backward_workspace_size.restype = sz
+    L.fa_status_string.argtypes = [i]
+    L.fa_status_string.restype = ctypes.c_char_p
+    return L
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fa_forward", "fa_backward", "fa_backward_workspace_size", "fa_check_device_status",
+              "fa_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (fa_\w+)", out))
+    for n in declared_functions():
+        assert n in exported, n
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert lib.fa_status_string(0) == b"FA_OK"
+    assert lib.fa_status_string(4) == b"FA_ERR_TIMEOUT"
+    assert lib.fa_status_string(99) == b"FA_UNKNOWN_STATUS"
+    assert lib.fa_version() == 100
+
+
+P = ctypes.c_void_p(0x10000)       # aligned, never dereferenced: every call below returns early
+MIS = ctypes.c_void_p(0x10008)      # 8-byte aligned only
+
+
+def fwd(lib, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=128, d=64, scale=0.125, causal=0, dtype=0):
+    return lib.fa_forward(q, k, v, o, lse, B, H, N, d, scale, causal, None, dtype, None, None)
+
+
+def test_forward_argument_checks(lib):
+    assert fwd(lib, d=96) == UNSUPPORTED
+    assert fwd(lib, d=32) == UNSUPPORTED
+    assert fwd(lib, dtype=7) == UNSUPPORTED
+    assert fwd(lib, B=-1) == INVALID
+    assert fwd(lib, N=-5) == INVALID
+    assert fwd(lib, scale=float("nan")) == INVALID
+    assert fwd(lib, scale=float("inf")) == INVALID
+    assert fwd(lib, q=None) == INVALID
+    assert fwd(lib, lse=None) == INVALID
+    assert fwd(lib, v=MIS) == INVALID
+    assert fwd(lib, o=MIS) == INVALID
+    # empty problems are no-ops
+    assert fwd(lib, N=0) == OK
+    assert fwd(lib, B=0, q=None) == OK
+    assert fwd(lib, H=0) == OK
+
+
+def test_backward_argument_checks(lib):
+    ws = lib.fa_backward_workspace_size(2, 3, 100, 64)
+    assert ws % 256 == 0 and ws >= 2 * 3 * 100 * 64 * 4 + 2 * 3 * 100 * 4
+    assert lib.fa_backward_workspace_size(0, 3, 100, 64) == 0
+
+    def bwd(dq=P, workspace=P, wsb=ws, d=64, N=100, dtype=0):
+        return lib.fa_backward(P, P, P, P, P, P, dq, P, P, 2, 3, N, d, 0.125, 0, None, dtype, None,
+                               workspace, wsb, None)
+    assert bwd(d=80) == UNSUPPORTED
+    assert bwd(dq=None) == INVALID
+    assert bwd(dq=MIS) == INVALID
+    assert bwd(workspace=None) == INVALID
+    assert bwd(workspace=ctypes.c_void_p(0x10010)) == INVALID     # not 256-byte aligned
+    assert bwd(wsb=ws - 4) == INVALID
+    assert bwd(N=0) == OK

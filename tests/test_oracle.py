@@ -346,3 +346,15 @@ def test_backward_zero_queries_closed_form():
     for j in range(N):
         expect = sum(do[i] / (i + 1) for i in range(j, N))
         assert np.max(np.abs(dV[0, 0, j] - expect)) < 1e-12
+
+
+def test_backward_row_samples_add_up():
+    """Splitting the query rows into samples: dQ rows match and dK, dV contributions add up."""
+    q, k, v, do = (_rand((1, 1, 150, 4), s) for s in (52, 53, 54, 55))
+    full = oracle.backward(q, k, v, do, 0.4, causal=True)
+    a = oracle.backward(q, k, v, do, 0.4, causal=True, rows=range(0, 61))
+    b = oracle.backward(q, k, v, do, 0.4, causal=True, rows=range(61, 150))
+    assert np.max(np.abs(a[0][:, :, :61] - full[0][:, :, :61])) < 1e-13
+    assert np.max(np.abs(b[0][:, :, 61:] - full[0][:, :, 61:])) < 1e-13
+    for i in (1, 2):
+        assert np.max(np.abs(a[i] + b[i] - full[i])) < 1e-12

@@ -1,0 +1,135 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded
+inputs, element by element, at sizes the oracle finishes in seconds (several tiles and a ragged
+tail) and on the workloads' own shapes; plus edge cases: empty and ragged inputs, fully masked
+rows, extreme logits, random tile masks."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import compare, f64, run_gpu
+from workloads import WORKLOADS, Workload, make_inputs, random_tile_mask
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(N, d, dtype="bf16", causal=False, B=2, H=3, pad=None, vs=1.0, seed=0):
+    w = Workload(f"t_{N}_{d}", B, H, N, d, dtype, causal=causal, value_scale=vs, pad_lengths=pad)
+    return make_inputs(w, seed=seed)
+
+
+# --- fp32 path -------------------------------------------------------------------------------
+
+def test_fp32_workload_n128_d64():
+    """The fp32 workload: B1 H1 N128 d64 non-causal, max-abs <= 1e-5 on O and LSE."""
+    x = make_inputs(WORKLOADS["fp32_n128_d64"])
+    compare(x, run_gpu(x, backward=True))
+
+
+@pytest.mark.parametrize("N,d,causal", [(1, 64, False), (100, 64, True), (129, 128, False),
+                                        (300, 128, True)])
+def test_fp32_shapes(N, d, causal):
+    x = _case(N, d, "fp32", causal, B=1, H=2, seed=N)
+    compare(x, run_gpu(x))
+
+
+# --- bf16 path: shapes, tails, masks ---------------------------------------------------------
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 2, 127, 128, 129, 255, 256, 257, 700])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_shapes(N, d, causal):
+    x = _case(N, d, "bf16", causal, seed=N * 7 + d + causal)
+    compare(x, run_gpu(x))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_key_padding(d, causal):
+    x = _case(600, d, "bf16", causal, B=4, H=2, pad=(1, 600), seed=11 + d)
+    x["kv_lens"] = torch.tensor([0, 1, 333, 600], dtype=torch.int32)   # includes an empty sequence
+    compare(x, run_gpu(x))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("density", [0.0, 0.3, 1.0])
+def test_bf16_random_tile_mask(d, causal, density):
+    x = _case(1000, d, "bf16", causal, B=1, H=2, seed=int(density * 10) + d)
+    bm = random_tile_mask(8, density, seed=d + causal)
+    if density > 0:
+        bm[3, :] = 0          # a tile row with nothing allowed: fully masked rows
+        bm[:, 0] = 1
+        bm[3, 0] = 0
+    x["block_mask"] = bm
+    compare(x, run_gpu(x))
+
+
+def test_bf16_mask_combination():
+    x = _case(900, 64, "bf16", True, B=3, H=2, seed=5)
+    x["kv_lens"] = torch.tensor([900, 450, 130], dtype=torch.int32)
+    x["block_mask"] = random_tile_mask(8, 0.5, seed=3)
+    x["block_mask"][torch.arange(8), torch.arange(8)] = 1
+    compare(x, run_gpu(x))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_extreme_logits(d):
+    """Scores pushed to about +-60 (page 3 asks for extreme logits to be covered)."""
+    x = _case(400, d, "bf16", False, B=1, H=2, seed=9)
+    s = (x["q"].float() @ x["k"].float().transpose(-1, -2)).abs().max().item()
+    x["scale"] = 60.0 / s
+    out = run_gpu(x)
+    for t in out.values():
+        assert torch.isfinite(t).all()
+    compare(x, out)
+
+
+def test_empty_problem_is_noop():
+    import exact_io_aware_23_gb300 as fa
+    q = torch.empty((2, 3, 0, 64), dtype=torch.bfloat16, device="cuda")
+    o, lse = fa.forward(q, q, q)
+    assert o.numel() == 0 and lse.numel() == 0
+
+
+# --- the workloads' own shapes ---------------------------------------------------------------
+
+def test_bert_large_pad_n512():
+    x = make_inputs(WORKLOADS["bert_large_pad_n512"])
+    compare(x, run_gpu(x))
+
+
+def test_gpt2_small_causal_n1024():
+    x = make_inputs(WORKLOADS["gpt2_small_causal_n1024"])
+    compare(x, run_gpu(x))
+
+
+@pytest.mark.parametrize("name", ["long_n16k_d128", "long_n16k_d128_causal"])
+def test_long_n16k_d128(name):
+    """Full fwd+bwd on all 16 heads on the GPU; oracle fwd+bwd on two heads and sampled rows
+    of every head; invariants on all heads."""
+    x = make_inputs(WORKLOADS[name])
+    out = run_gpu(x)
+    compare(x, out, heads=[0, 15])
+    rows = np.sort(np.random.default_rng(0).choice(16384, 256, replace=False))
+    compare(x, out, heads=list(range(1, 15)), rows=rows, backward=False)
+    _invariants(x, out)
+
+
+def test_block_sparse_n64k_d64():
+    x = make_inputs(WORKLOADS["block_sparse_n64k_d64"])
+    out = run_gpu(x)
+    compare(x, out, heads=[0])
+    rows = np.sort(np.random.default_rng(1).choice(65536, 512, replace=False))
+    compare(x, out, heads=list(range(1, 8)), rows=rows, backward=False)
+    _invariants(x, out)
+
+
+def _invariants(x, out):
+    """sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i (every row has an allowed key here)."""
+    dk, dv, do = f64(out["dk"]), f64(out["dv"]), f64(x["do"])
+    scale_k = np.sqrt(np.mean(dk ** 2)) * math.sqrt(dk.shape[2])
+    assert np.max(np.abs(dk.sum(axis=2))) <= 5e-2 * scale_k
+    ref = do.sum(axis=2)
+    assert np.max(np.abs(dv.sum(axis=2) - ref)) <= 2e-2 * np.max(np.abs(ref)) + 1e-3 * math.sqrt(dv.shape[2])
