@@ -7,6 +7,7 @@
 #include <atomic>
 
 #include "fa_internal.cuh"
+#include "fa_sm103.cuh"
 
 namespace {
 
@@ -34,7 +35,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 fa_status check_common(int B, int H, int N, int d, float scale, fa_dtype dtype) {
   if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
-  if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (!isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (H > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
@@ -88,7 +89,7 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
   a.kv_lens = kv_lens; a.dbg = knobs();
   if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = fa::launch_fwd_simt(a, dtype, s);
+  cudaError_t e = dtype == FA_BF16 ? fa::launch_fwd_sm103(a, s) : fa::launch_fwd_simt(a, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -126,7 +127,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = fa::launch_bwd_preprocess(a, dtype, s);
   if (e == cudaSuccess)
-    e = fa::launch_bwd_simt(a, dtype, s);
+    e = dtype == FA_BF16 ? fa::launch_bwd_sm103(a, s) : fa::launch_bwd_simt(a, dtype, s);
   if (e == cudaSuccess) e = fa::launch_bwd_dq_convert(a, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -1,0 +1,449 @@
+// Tensor-core attention backward for sm_103a (bf16 in, fp32 accumulate), d in {64, 128}.
+//
+// The method ("FlashAttention paper story", backward paragraph; "FlashAttention: Exact Attention
+// with Less GPU Memory", "Tiling, and paying arithmetic to avoid memory"): only the per-row
+// softmax statistic is kept from the forward; the backward recomputes the scores and P tile by
+// tile on chip.  With D_i = rowsum(dO_i * O_i) (computed by the preprocess kernel):
+//     P = exp(scale*S - LSE),  dV += P^T dO,  dP = dO V^T,  dS = P * (dP - D),
+//     dK += scale * dS^T Q,  dQ += scale * dS K.
+//
+// GB300 design: one CTA per 128-key tile j of one (b, h) slice, 320 threads, looping over every
+// live 128-row query tile i.  The transposed products keep the key rows on the TMEM lanes, so
+// one thread owns one key row of S^T, dP^T, P^T and dS^T:
+//   warp 8      TMA producer: K_j, V_j once; Q_i, dO_i through a two-stage ring, with the
+//               tile's LSE (as a log2-domain bias) and D vectors staged beside them.
+//   warp 9      MMA issuer: S^T = K_j Q_i^T and dP^T = V_j dO_i^T (SS), then
+//               dV += P^T dO_i and dK += dS^T Q_i (TS: P^T, dS^T read from TMEM) and
+//               dQ_i = dS K_j (SS: dS staged in shared memory), two N = d/2 halves.
+//   warps 0-7   two warpgroups, query columns [0,64) and [64,128): P^T and dS^T in registers,
+//               written back to TMEM as bf16 and dS also to shared memory; then they add the
+//               tile's dQ into the fp32 workspace with vector atomics.
+//   TMEM d=128: dV [0,128) dK [128,256) X=S^T [256,384) Y=dP^T [384,512); P^T packed in
+//               X[0,64), dS^T packed in Y[0,64), dQ halves in X[64,128) and Y[64,128).
+//   TMEM d=64:  dV [0,64) dK [64,128) X [128,256) Y [256,384) dQ [384,448).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "fa_internal.cuh"
+#include "fa_sm103.cuh"
+#include "ptx_sm103.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int BM = 128;          // query rows per tile
+constexpr int BN = 128;          // keys per CTA
+constexpr int kThreads = 320;
+constexpr int kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct Cfg {
+  static constexpr int kTile = 128 * D * 2;                  // one 128-row operand tile
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTile;
+  static constexpr int kQ0 = kV + kTile;                     // stage s: Q at kQ0 + s*2*kTile
+  static constexpr int kDS = kQ0 + 4 * kTile;                // dS [128 keys][128 queries] bf16
+  static constexpr int kVec = kDS + 128 * 128 * 2;           // stage s: lse2[128], delta[128]
+  static constexpr int kBar = kVec + 2 * 2 * 128 * 4;
+  static constexpr int kSmem = kBar + 256;
+  // TMEM columns
+  static constexpr uint32_t kDV = 0, kDK = D, kX = 2 * D, kY = 2 * D + 128;
+  static constexpr uint32_t kIdescST = ptx::idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+  static constexpr uint32_t kIdescAcc = ptx::idesc_bf16_f32(128, D, false, true);    // dV, dK
+  static constexpr uint32_t kIdescDQ = ptx::idesc_bf16_f32(128, 64, true, true);     // dQ parts
+  static constexpr int kDQParts = D / 64;                    // N = 64 columns of d per part
+};
+
+struct Bars {
+  uint64_t kv_full;
+  uint64_t st_full[2];
+  uint64_t st_empty[2];
+  uint64_t s_full;
+  uint64_t dp_full;
+  uint64_t s_read;
+  uint64_t dp_read;
+  uint64_t ds_ready;
+  uint64_t dq_full;
+  uint64_t dq_free;
+  uint64_t acc_done;
+  uint32_t tmem_base;
+};
+
+enum : int { kNone = 0, kPartial = 1, kFull = 2 };
+
+struct Geo {
+  int k0, N, kv_lim, causal, T;
+  const uint8_t* bm;
+  int i_begin, i_end;    // query tiles that may be live
+  __device__ int kind(int i) const {
+    const int r0 = i * BM, r1 = min(r0 + BM, N) - 1;
+    const int c0 = k0, c1 = k0 + BN - 1;
+    if (bm != nullptr && bm[(size_t)i * T + k0 / BN] == 0) return kNone;
+    if (c0 >= kv_lim || (causal && c0 > r1)) return kNone;
+    if (c1 < kv_lim && (!causal || c1 <= r0)) return kFull;
+    return kPartial;
+  }
+  __device__ int next(int i) const {
+    while (i < i_end && kind(i) == kNone) ++i;
+    return i;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                 BwdArgs a) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if ((ptx::smem_u32(smem) & 1023u) != 0) {      // the operand tiles need 1 KB alignment
+    if (threadIdx.x == 0) atomicExch(a.err, 2);
+    return;
+  }
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kBar);
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int bh = b * a.H + h;
+  const uint32_t lim_ms = a.dbg.wait_limit_ms;
+
+  Geo g;
+  g.k0 = blockIdx.x * BN;
+  g.N = a.N;
+  int kvl = a.N;
+  if (a.kv_lens != nullptr) kvl = max(0, min(a.N, (int)a.kv_lens[b]));
+  g.kv_lim = kvl;
+  g.causal = a.causal;
+  g.T = a.n_tiles;
+  g.bm = a.block_mask;
+  g.i_begin = a.causal ? blockIdx.x : 0;
+  g.i_end = g.k0 < g.kv_lim ? (a.N + BM - 1) / BM : 0;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bars->kv_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->st_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->st_empty[s]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->s_read), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->dp_read), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->ds_ready), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->dq_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->dq_free), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->acc_done), 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------- producer (whole warp) --------------------------------------
+    bool ok = true;
+    int n = 0;
+    if (g.next(g.i_begin) < g.i_end) {
+      if (lane == 0) {
+        const uint32_t kb = ptx::smem_u32(&bars->kv_full);
+        ptx::mbar_arrive_expect_tx(kb, 2 * C::kTile);
+        for (int hh = 0; hh < D / 64; ++hh) {
+          ptx::tma_load_3d(sbase + C::kK + hh * 128 * 128, &tmK, kb, hh * 64, g.k0, bh);
+          ptx::tma_load_3d(sbase + C::kV + hh * 128 * 128, &tmV, kb, hh * 64, g.k0, bh);
+        }
+      }
+      for (int i = g.next(g.i_begin); i < g.i_end && ok; i = g.next(i + 1), ++n) {
+        const int st = n & 1;
+        const uint32_t ph = (n >> 1) & 1;
+        if (lane == 0) ok = ptx::mbar_wait(ptx::smem_u32(&bars->st_empty[st]), ph ^ 1, lim_ms, a.err);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        // LSE (as a log2-domain bias; +inf where P must vanish) and D for the tile's rows
+        float* lse2 = reinterpret_cast<float*>(smem + C::kVec + st * 1024);
+        float* dl = lse2 + 128;
+        for (int r = lane; r < 128; r += 32) {
+          const int q = i * BM + r;
+          float L = q < a.N ? a.lse[(size_t)bh * a.N + q] : -INFINITY;
+          lse2[r] = L == -INFINITY ? INFINITY : L * kLog2e;
+          dl[r] = q < a.N ? a.delta[(size_t)bh * a.N + q] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t fb = ptx::smem_u32(&bars->st_full[st]);
+          ptx::mbar_arrive_expect_tx(fb, 2 * C::kTile);
+          const uint32_t sq = sbase + C::kQ0 + st * 2 * C::kTile;
+          for (int hh = 0; hh < D / 64; ++hh) {
+            ptx::tma_load_3d(sq + hh * 128 * 128, &tmQ, fb, hh * 64, i * BM, bh);
+            ptx::tma_load_3d(sq + C::kTile + hh * 128 * 128, &tmDO, fb, hh * 64, i * BM, bh);
+          }
+        }
+      }
+      if (lane == 0) {   // drain: copies in flight must land before shared memory is released
+        ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, lim_ms, a.err);
+        for (int m = max(0, n - 2); m < n; ++m)
+          ptx::mbar_wait(ptx::smem_u32(&bars->st_full[m & 1]), (m >> 1) & 1, lim_ms, a.err);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------- MMA issuer -------------------------------------------------
+    if (lane == 0) {
+      bool ok = true;
+      int n = 0;
+      if (g.next(g.i_begin) < g.i_end) {
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, lim_ms, a.err);
+        for (int i = g.next(g.i_begin); i < g.i_end && ok; i = g.next(i + 1), ++n) {
+          const int st = n & 1;
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->st_full[st]), (n >> 1) & 1, lim_ms, a.err);
+          if (ok && n > 0 && D == 128)   // X, Y hold the previous tile's dQ until it is drained
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->dq_free), (n - 1) & 1, lim_ms, a.err);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint32_t sq = sbase + C::kQ0 + st * 2 * C::kTile;
+          const uint32_t sdo = sq + C::kTile;
+          // S^T = K Q^T, dP^T = V dO^T (K-major operands, k-steps of 16 along d)
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+            ptx::mma_ss(tmem + C::kX, ptx::sdesc_sw128(sbase + C::kK + off, 16, 1024),
+                        ptx::sdesc_sw128(sq + off, 16, 1024), C::kIdescST, kk > 0);
+          }
+          ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+            ptx::mma_ss(tmem + C::kY, ptx::sdesc_sw128(sbase + C::kV + off, 16, 1024),
+                        ptx::sdesc_sw128(sdo + off, 16, 1024), C::kIdescST, kk > 0);
+          }
+          ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_ready), n & 1, lim_ms, a.err);
+          if (ok && n > 0 && D == 64)
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->dq_free), (n - 1) & 1, lim_ms, a.err);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          // dV += P^T dO, dK += dS^T Q: A from TMEM (16 queries = 8 packed columns per step),
+          // B = dO / Q with the query index as K (MN-major, 16 rows = 2048 bytes per step)
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk) {
+            const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
+            ptx::mma_ts(tmem + C::kDV, tmem + C::kX + kk * 8,
+                        ptx::sdesc_sw128(sdo + kk * 2048, 128 * 128, 1024), C::kIdescAcc, acc);
+            ptx::mma_ts(tmem + C::kDK, tmem + C::kY + kk * 8,
+                        ptx::sdesc_sw128(sq + kk * 2048, 128 * 128, 1024), C::kIdescAcc, acc);
+          }
+          // dQ_i = dS K_j, 64 columns of d per part: A = dS (queries x keys, query-major in
+          // shared memory), B = K (keys x d, d-major); 16 keys = 2048 bytes per step.
+#pragma unroll
+          for (int part = 0; part < C::kDQParts; ++part) {
+            const uint32_t dst = D == 128 ? (part == 0 ? C::kX + 64 : C::kY + 64) : 384;
+            const uint32_t kb = sbase + C::kK + part * 128 * 128;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              ptx::mma_ss(tmem + dst, ptx::sdesc_sw128(sbase + C::kDS + kk * 2048, 128 * 128, 1024),
+                          ptx::sdesc_sw128(kb + kk * 2048, 128 * 128, 1024), C::kIdescDQ, kk > 0);
+          }
+          ptx::mma_commit(ptx::smem_u32(&bars->dq_full));
+          ptx::mma_commit(ptx::smem_u32(&bars->st_empty[st]));
+        }
+      }
+      ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
+      ptx::mbar_wait(ptx::smem_u32(&bars->acc_done), 0, lim_ms, a.err);
+    }
+  } else {
+    // ------------------------------- compute warpgroups -----------------------------------------
+    const int wg = warp / 4, sub = warp % 4;
+    const int kr = sub * 32 + lane;                  // key row within the tile (TMEM lane)
+    const int key = g.k0 + kr;
+    const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
+    const float c = a.scale * kLog2e;
+    const bool key_ok = key < g.kv_lim;
+    bool ok = true;
+    int n = 0;
+    for (int i = g.next(g.i_begin); i < g.i_end; i = g.next(i + 1), ++n) {
+      const int st = n & 1;
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->st_full[st]), (n >> 1) & 1, lim_ms, a.err);
+      if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full), n & 1, lim_ms, a.err);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const float* lse2 = reinterpret_cast<const float*>(smem + C::kVec + st * 1024) + wg * 64;
+      const float* dl = lse2 + 128;
+      const int kind = g.kind(i);
+      const int q0 = i * BM + wg * 64;               // first query column of this warpgroup
+      // P^T for this thread's key row over 64 query columns
+      float p[64];
+      {
+        uint32_t raw[32];
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          ptx::tmem_ld32(tmem + lane_off + C::kX + wg * 64 + hc * 32, raw);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = hc * 32 + e;
+            float v = ptx::ex2(fmaf(__uint_as_float(raw[e]), c, -lse2[col]));
+            if (kind == kPartial) {
+              const bool allowed = key_ok && (!g.causal || key <= q0 + col);
+              v = allowed ? v : 0.f;
+            }
+            p[col] = v;
+          }
+        }
+      }
+      // all of S^T is read (by both warpgroups) before P^T overwrites part of it
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_read));
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_read), n & 1, lim_ms, a.err);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack_bf16(p[2 * e], p[2 * e + 1]);
+        ptx::tmem_st32(tmem + lane_off + C::kX + wg * 32, pk);
+      }
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->dp_full), n & 1, lim_ms, a.err);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      // dS^T = P^T * (dP^T - D)
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        uint32_t raw[32];
+        ptx::tmem_ld32(tmem + lane_off + C::kY + wg * 64 + hc * 32, raw);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = hc * 32 + e;
+          p[col] = p[col] * (__uint_as_float(raw[e]) - dl[col]);
+        }
+      }
+      ptx::tc_fence_before();                         // all of dP^T read before dS^T overwrites Y
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->dp_read));
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->dp_read), n & 1, lim_ms, a.err);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack_bf16(p[2 * e], p[2 * e + 1]);
+        ptx::tmem_st32(tmem + lane_off + C::kY + wg * 32, pk);
+        // dS into shared memory, query-major 128-byte-swizzled: row = key, 64 queries per atom
+        uint8_t* row = smem + C::kDS + wg * (128 * 128) + kr * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint4 w = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          *reinterpret_cast<uint4*>(row + ((ch ^ (kr & 7)) << 4)) = w;
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_ready));
+      // dQ of this query tile: lane = query row; this warpgroup takes half of d
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->dq_full), n & 1, lim_ms, a.err);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      {
+        const int q = i * BM + kr;
+        const uint32_t src = D == 128 ? (wg == 0 ? C::kX + 64 : C::kY + 64) : 384 + wg * 32;
+        float* dst = a.dq_acc + ((size_t)bh * a.N + q) * D + wg * (D / 2);
+#pragma unroll
+        for (int hc = 0; hc < D / 64; ++hc) {
+          uint32_t raw[32];
+          ptx::tmem_ld32(tmem + lane_off + src + hc * 32, raw);
+          ptx::tmem_wait_ld();
+          if (q < a.N) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              atomicAdd(reinterpret_cast<float4*>(dst + hc * 32 + e),
+                        make_float4(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1]),
+                                    __uint_as_float(raw[e + 2]), __uint_as_float(raw[e + 3])));
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->dq_free));
+    }
+    // ------------------------------- epilogue: dV (warpgroup 0), dK (warpgroup 1) --------------
+    const bool have = ok && n > 0;
+    if (have) {
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_done), 0, lim_ms, a.err);
+      ptx::tc_fence_after();
+    }
+    const float mult = wg == 0 ? 1.f : a.scale;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(wg == 0 ? a.dv : a.dk) + ((size_t)bh * a.N + key) * D;
+    const uint32_t src = wg == 0 ? C::kDV : C::kDK;
+#pragma unroll 1
+    for (int hc = 0; hc < D / 32; ++hc) {
+      uint32_t raw[32];
+      if (have && ok) {
+        ptx::tmem_ld32(tmem + lane_off + src + hc * 32, raw);
+        ptx::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) raw[e] = 0u;
+      }
+      if (key < a.N) {
+        uint4* dst = reinterpret_cast<uint4*>(out + hc * 32);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          uint4 w;
+          w.x = ptx::pack_bf16(__uint_as_float(raw[8 * v4 + 0]) * mult, __uint_as_float(raw[8 * v4 + 1]) * mult);
+          w.y = ptx::pack_bf16(__uint_as_float(raw[8 * v4 + 2]) * mult, __uint_as_float(raw[8 * v4 + 3]) * mult);
+          w.z = ptx::pack_bf16(__uint_as_float(raw[8 * v4 + 4]) * mult, __uint_as_float(raw[8 * v4 + 5]) * mult);
+          w.w = ptx::pack_bf16(__uint_as_float(raw[8 * v4 + 6]) * mult, __uint_as_float(raw[8 * v4 + 7]) * mult);
+          dst[v4] = w;
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 9) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH) {
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int D>
+cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
+  CUtensorMap mq, mk, mv, mdo;
+  const int BH = a.B * a.H;
+  cudaError_t e;
+  if ((e = make_map(&mq, a.q, D, a.N, BH)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, a.k, D, a.N, BH)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.v, D, a.N, BH)) != cudaSuccess) return e;
+  if ((e = make_map(&mdo, a.dO, D, a.N, BH)) != cudaSuccess) return e;
+  auto kern = bwd_sm103_kernel<D>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.N + BN - 1) / BN, a.H, a.B);
+  kern<<<grid, kThreads, Cfg<D>::kSmem, s>>>(mq, mk, mv, mdo, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_sm103(const BwdArgs& a, cudaStream_t s) {
+  return a.d == 64 ? launch<64>(a, s) : launch<128>(a, s);
+}
+
+}  // namespace fa

@@ -1,0 +1,422 @@
+// Tensor-core attention forward for sm_103a (bf16 in, fp32 accumulate), d in {64, 128}.
+//
+// The method ("FlashAttention paper story", tiling and online-softmax paragraphs; "FlashAttention：
+// 让精确注意力服从内存层次", section "Online softmax" and its merge law): Q is cut into row
+// tiles, K/V into column tiles; each query row keeps a running maximum m and normaliser l and an
+// un-normalised output; scores and probabilities of one tile live only on chip.  O = u / l and
+// LSE = m + ln l are written once at the end.
+//
+// GB300 design (one CTA = two 128-row Q tiles of one (b, h) slice, 384 threads):
+//   warp 8      TMA producer: Q tiles once, then K_j, V_j for every live key tile j through a
+//               ring of shared-memory slots (mbarrier full/empty pairs).  Masked tiles are never
+//               loaded ("FlashAttention paper story", block-sparse paragraph).
+//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T (SS MMA, 128 x 128 x d) into TMEM, and
+//               O_t += P_t V_j (TS MMA: P_t read from TMEM, V_j from shared memory).
+//   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1: each thread owns one query row
+//               (one TMEM lane), reads its 128 scores, masks, updates m and l with exp2, and
+//               writes P as bf16 back into the TMEM columns of S.  The two tiles ping-pong, so
+//               one tile's softmax overlaps the other tile's MMAs.
+//   TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [256+d,256+2d).
+// The running maximum is only raised when a row's new maximum exceeds it by more than
+// 2^8 (kRescaleLog2): P and l use the same stale maximum, so the result is unchanged and the O
+// rescale (a TMEM read-modify-write) is rare.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "fa_internal.cuh"
+#include "fa_sm103.cuh"
+#include "ptx_sm103.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int BM = 128;          // rows per Q tile
+constexpr int BN = 128;          // keys per K/V tile
+constexpr int kThreads = 384;
+constexpr int kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+enum : int { kNone = 0, kPartial = 1, kFull = 2 };
+
+template <int D>
+struct Cfg {
+  static constexpr int kTileBytes = BN * D * 2;                 // one K or V tile; one Q tile
+  static constexpr int kSlots = D == 128 ? 5 : 8;               // K/V ring depth
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
+  static constexpr int kSmem = kBarOff + 256 + 1024;            // + barriers + alignment slack
+  static constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(BM, BN, false, false);
+  static constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(BM, D, false, true);
+};
+
+struct Bars {            // all mbarriers of one CTA (8 bytes each)
+  uint64_t q_full;
+  uint64_t s_full[2];
+  uint64_t p_ready[2];
+  uint64_t pv_done[2];
+  uint64_t mma_done;
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint32_t tmem_base;
+};
+
+// Per-CTA tile geometry: which key tiles exist and how each Q tile must treat them.
+struct Geo {
+  int q0;          // first query row of Q tile 0
+  int N, kv_lim;   // keys with j >= kv_lim are masked (padding and tail)
+  int causal;
+  const uint8_t* bm;
+  int T;
+  int j_end;       // key tiles [0, j_end) may be live
+
+  __device__ int kind(int t, int j) const {
+    const int r0 = q0 + t * BM;
+    if (r0 >= N) return kNone;
+    const int r1 = min(r0 + BM, N) - 1;
+    const int c0 = j * BN, c1 = c0 + BN - 1;
+    if (bm != nullptr && bm[(size_t)(r0 / BM) * T + j] == 0) return kNone;
+    if (c0 >= kv_lim || (causal && c0 > r1)) return kNone;
+    if (c1 < kv_lim && (!causal || c1 <= r0)) return kFull;
+    return kPartial;
+  }
+  __device__ bool live(int j) const { return kind(0, j) != kNone || kind(1, j) != kNone; }
+  __device__ int next(int j) const {
+    while (j < j_end && !live(j)) ++j;
+    return j;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, FwdArgs a) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOff);
+  const uint32_t sQ = ptx::smem_u32(smem + C::kQOff);
+  const uint32_t sKV = ptx::smem_u32(smem + C::kKVOff);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int n_pairs = gridDim.x;
+  // heavier (later) query tiles first when causal
+  const int pair = a.causal ? n_pairs - 1 - blockIdx.x : blockIdx.x;
+  const int bh = b * a.H + h;
+
+  Geo g;
+  g.q0 = pair * 2 * BM;
+  g.N = a.N;
+  int kvl = a.N;
+  if (a.kv_lens != nullptr) kvl = max(0, min(a.N, (int)a.kv_lens[b]));
+  g.kv_lim = kvl;
+  g.causal = a.causal;
+  g.bm = a.block_mask;
+  g.T = a.n_tiles;
+  {
+    int last_key = g.kv_lim;
+    if (a.causal) last_key = min(last_key, min(g.q0 + 2 * BM, a.N));
+    g.j_end = (last_key + BN - 1) / BN;
+  }
+  const uint32_t lim_ms = a.dbg.wait_limit_ms;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(ptx::smem_u32(&bars->s_full[t]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->p_ready[t]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->pv_done[t]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bars->mma_done), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->kv_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[s]), 1);
+    }
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp >= 8) {
+    ptx::regs_dec<56>();
+    if (warp == 8 && lane == 0) {
+      // ------------------------------- TMA producer -------------------------------------------
+      ptx::tma_prefetch_desc(&tmQ);
+      ptx::tma_prefetch_desc(&tmK);
+      ptx::tma_prefetch_desc(&tmV);
+      const uint32_t qbar = ptx::smem_u32(&bars->q_full);
+      ptx::mbar_arrive_expect_tx(qbar, 2 * C::kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int hh = 0; hh < D / 64; ++hh)
+          ptx::tma_load_3d(sQ + t * C::kTileBytes + hh * BM * 128, &tmQ, qbar, hh * 64, g.q0 + t * BM, bh);
+      int n = 0;
+      bool ok = true;
+      for (int j = g.next(0); j < g.j_end && ok; j = g.next(j + 1)) {
+        for (int kind = 0; kind < 2 && ok; ++kind, ++n) {
+          const int slot = n % C::kSlots;
+          const uint32_t ph = (n / C::kSlots) & 1;
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[slot]), ph ^ 1, lim_ms, a.err);
+          if (!ok) break;
+          if (a.dbg.inject == 1 && n == 0) continue;      // test hook: never deliver this tile
+          const uint32_t fb = ptx::smem_u32(&bars->kv_full[slot]);
+          ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
+          const CUtensorMap* m = kind == 0 ? &tmK : &tmV;
+          for (int hh = 0; hh < D / 64; ++hh)
+            ptx::tma_load_3d(sKV + slot * C::kTileBytes + hh * BN * 128, m, fb, hh * 64, j * BN, bh);
+        }
+      }
+      // Drain: every copy this CTA issued must have landed before shared memory is released.
+      ptx::mbar_wait(qbar, 0, lim_ms, a.err);
+      for (int m = max(0, n - C::kSlots); m < n; ++m) {
+        if (a.dbg.inject == 1 && m == 0) continue;
+        ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[m % C::kSlots]), (m / C::kSlots) & 1, lim_ms, a.err);
+      }
+    } else if (warp == 9 && lane == 0) {
+      // ------------------------------- MMA issuer ---------------------------------------------
+      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, lim_ms, a.err);
+      ptx::tc_fence_after();
+      int n = 0, idx = 0;
+      int prev_v = -1;
+      uint32_t prev_vph = 0;
+      for (int j = g.next(0); j < g.j_end && ok; j = g.next(j + 1), ++idx) {
+        const int kslot = n % C::kSlots;
+        const uint32_t kph = (n / C::kSlots) & 1;
+        ++n;
+        const int vslot = n % C::kSlots;
+        const uint32_t vph = (n / C::kSlots) & 1;
+        ++n;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[kslot]), kph, lim_ms, a.err);
+        if (ok && idx > 0) ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[prev_v]), prev_vph, lim_ms, a.err);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (idx > 0) {
+            // O_t += P_t V_{j_prev}: P_t of the previous key tile sits in S_t's columns.
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_ready[t]), (idx - 1) & 1, lim_ms, a.err);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint32_t vbase = sKV + prev_v * C::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint64_t bdesc = ptx::sdesc_sw128(vbase + kk * 16 * 128, BN * 128, 1024);
+              ptx::mma_ts(tmem + 256 + t * D, tmem + t * BN + kk * 8, bdesc, C::kIdescO,
+                          (idx > 1 || kk > 0) ? 1u : 0u);
+            }
+            if (t == 1) ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[prev_v]));
+          }
+          // S_t = Q_t K_j^T
+          const uint32_t qbase = sQ + t * C::kTileBytes;
+          const uint32_t kbase = sKV + kslot * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+            const uint64_t adesc = ptx::sdesc_sw128(qbase + off, 16, 1024);
+            const uint64_t bdesc = ptx::sdesc_sw128(kbase + off, 16, 1024);
+            ptx::mma_ss(tmem + t * BN, adesc, bdesc, C::kIdescS, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_u32(&bars->s_full[t]));
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[kslot]));
+        prev_v = vslot;
+        prev_vph = vph;
+      }
+      if (ok && idx > 0) {
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[prev_v]), prev_vph, lim_ms, a.err);
+        ptx::tc_fence_after();
+        for (int t = 0; t < 2 && ok; ++t) {
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_ready[t]), (idx - 1) & 1, lim_ms, a.err);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint32_t vbase = sKV + prev_v * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t bdesc = ptx::sdesc_sw128(vbase + kk * 16 * 128, BN * 128, 1024);
+            ptx::mma_ts(tmem + 256 + t * D, tmem + t * BN + kk * 8, bdesc, C::kIdescO,
+                        (idx > 1 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_u32(&bars->pv_done[t]));
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[prev_v]));
+      }
+      // every MMA this thread issued has finished before TMEM and shared memory are released
+      ptx::mma_commit(ptx::smem_u32(&bars->mma_done));
+      ptx::mbar_wait(ptx::smem_u32(&bars->mma_done), 0, lim_ms, a.err);
+    }
+  } else {
+    // ------------------------------- softmax warpgroups -----------------------------------------
+    ptx::regs_inc<208>();
+    const int t = warp / 4;
+    const int sub = warp % 4;
+    const int r = sub * 32 + lane;                  // TMEM lane == row within the Q tile
+    const int i = g.q0 + t * BM + r;                // query row in the head
+    const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * BN;
+    const uint32_t tO = tmem + lane_off + 256 + t * D;
+    const float c = a.scale * kLog2e;               // scores -> log2 domain
+    int row_lim = min(g.kv_lim, a.N);
+    if (a.causal) row_lim = min(row_lim, i + 1);
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    int idx = 0;
+    for (int j = g.next(0); j < g.j_end; j = g.next(j + 1), ++idx) {
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[t]), idx & 1, lim_ms, a.err);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int kind = g.kind(t, j);
+      uint32_t pk[32];
+      if (kind == kNone) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = 0u;
+        ptx::tmem_st32(tS, pk);
+        ptx::tmem_st32(tS + 32, pk);
+      } else {
+        float s[BN];
+        {
+          uint32_t raw[32];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            ptx::tmem_ld32(tS + q4 * 32, raw);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s[q4 * 32 + e] = __uint_as_float(raw[e]);
+          }
+        }
+        if (kind == kPartial) {
+          const int lim = row_lim - j * BN;
+#pragma unroll
+          for (int e = 0; e < BN; ++e) s[e] = e < lim ? s[e] : -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int e = 1; e < BN; ++e) mx = fmaxf(mx, s[e]);
+        const float m_cand = mx * c;
+        const bool need = m_cand > m_run + kRescaleLog2;   // false when the row is still empty
+        const float alpha = need ? ptx::ex2(m_run - m_cand) : 1.f;
+        if (__any_sync(0xffffffffu, need) && idx > 0) {
+          // O_t *= alpha for this warp's rows (PV of the previous tile has completed: the
+          // commit that signalled s_full was issued after it).
+#pragma unroll 1
+          for (int q4 = 0; q4 < D / 32; ++q4) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + q4 * 32, o);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st32(tO + q4 * 32, o);
+          }
+        }
+        if (need) {
+          l_run *= alpha;
+          m_run = m_cand;
+        }
+        const float msub = m_run == -INFINITY ? 0.f : m_run;
+        float lsum = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float p0 = ptx::ex2(fmaf(s[half * 64 + 2 * e], c, -msub));
+            const float p1 = ptx::ex2(fmaf(s[half * 64 + 2 * e + 1], c, -msub));
+            lsum += p0 + p1;
+            pk[e] = ptx::pack_bf16(p0, p1);
+          }
+          ptx::tmem_st32(tS + half * 32, pk);
+        }
+        l_run += lsum;
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_ready[t]));
+    }
+    // ------------------------------- epilogue ----------------------------------------------------
+    const bool have_o = ok && idx > 0;
+    if (have_o) {
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->pv_done[t]), 0, lim_ms, a.err);
+      ptx::tc_fence_after();
+    }
+    const bool any = l_run > 0.f;
+    const float inv = any ? 1.f / l_run : 0.f;
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) + ((size_t)bh * a.N + i) * D;
+#pragma unroll 1
+    for (int q4 = 0; q4 < D / 32; ++q4) {
+      uint32_t o[32];
+      if (have_o && ok) {
+        ptx::tmem_ld32(tO + q4 * 32, o);
+        ptx::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
+      if (i < a.N) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          uint4 w;
+          w.x = ptx::pack_bf16(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+          w.y = ptx::pack_bf16(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+          w.z = ptx::pack_bf16(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+          w.w = ptx::pack_bf16(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+          dst[v4] = w;
+        }
+      }
+    }
+    if (i < a.N) a.lse[(size_t)bh * a.N + i] = any ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 9) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---- host side -----------------------------------------------------------------------------------
+
+cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH) {
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int D>
+cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
+  CUtensorMap mq, mk, mv;
+  const int BH = a.B * a.H;
+  cudaError_t e;
+  if ((e = make_map(&mq, a.q, D, a.N, BH)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, a.k, D, a.N, BH)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.v, D, a.N, BH)) != cudaSuccess) return e;
+  auto kern = fwd_sm103_kernel<D>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
+  if (e != cudaSuccess) return e;
+  // The warp groups re-split the CTA's registers (4 warps down to 56, 8 warps up to 208 per
+  // thread); that only completes if the launch holds at least that many registers.
+  cudaFuncAttributes fattr;
+  if ((e = cudaFuncGetAttributes(&fattr, kern)) != cudaSuccess) return e;
+  if (fattr.numRegs * kThreads < 128 * 56 + 256 * 208) return cudaErrorInvalidConfiguration;
+  dim3 grid((a.N + 2 * BM - 1) / (2 * BM), a.H, a.B);
+  kern<<<grid, kThreads, Cfg<D>::kSmem, s>>>(mq, mk, mv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_sm103(const FwdArgs& a, cudaStream_t s) {
+  return a.d == 64 ? launch<64>(a, s) : launch<128>(a, s);
+}
+
+}  // namespace fa

@@ -1,0 +1,45 @@
+// TMA descriptor encoding.  cuTensorMapEncodeTiled is a driver API function; it is looked up
+// through the runtime's entry-point query so the library does not link against libcuda and
+// loads on machines without a GPU driver.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "fa_sm103.cuh"
+
+namespace fa {
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+
+EncodeFn g_encode = nullptr;
+std::once_flag g_once;
+
+void resolve() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<EncodeFn>(fn);
+}
+
+}  // namespace
+
+cudaError_t encode_tensor_map(CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank,
+                              const void* base, const cuuint64_t* dims, const cuuint64_t* strides,
+                              const cuuint32_t* box, const cuuint32_t* elem_strides,
+                              CUtensorMapSwizzle swizzle) {
+  std::call_once(g_once, resolve);
+  if (g_encode == nullptr) return cudaErrorNotSupported;
+  CUresult r = g_encode(m, dt, rank, const_cast<void*>(base), dims, strides, box, elem_strides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -48,7 +48,7 @@ extern "C" {
 
 typedef enum {
   FA_OK = 0,
-  FA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer, bad scale */
+  FA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer, scale <= 0 */
   FA_ERR_UNSUPPORTED = 2,   /* head dim other than 64/128, unknown dtype, size limits */
   FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or a launch failed */
   FA_ERR_TIMEOUT = 4        /* a kernel's bounded wait ran out (see fa_check_device_status) */
@@ -65,6 +65,7 @@ typedef enum {
  *   o          : output, [B,H,N,d] in `dtype` (must not alias q/k/v)
  *   lse        : output, [B,H,N] fp32, ln of the softmax normaliser of each query row
  *   scale      : multiplies q.k before the softmax (1/sqrt(d) for standard attention); finite
+ *                and > 0
  *   causal     : nonzero = mask keys j > i
  *   block_mask : nullable; [T,T] uint8 tile mask (0 = tile skipped)
  *   kv_lens    : nullable; [B] int32 valid key count per sequence (keys j >= kv_lens[b]

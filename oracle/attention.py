@@ -143,11 +143,14 @@ def probabilities(q, k, scale: float, causal: bool = False, kv_len=None, block_m
 
 def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, block_mask=None,
              heads: Optional[Sequence[int]] = None, return_delta: bool = False,
-             rows: Optional[Sequence[int]] = None):
+             rows: Optional[Sequence[int]] = None, o=None):
     """Explicit-gradient backward of dense masked attention, fp64.
 
-    Returns (dQ, dK, dV), each [B, len(heads), N, d]; with ``return_delta`` also D [B,H',N]
-    where D_i = sum_j P_ij dP_ij.  Rows whose LSE is -inf contribute nothing.  ``rows``
+    Returns (dQ, dK, dV), each [B, len(heads), N, d]; with ``return_delta`` also D [B,H',N].
+    D_i = sum_j P_ij dP_ij, the exact gradient's row term.  When the forward output ``o``
+    ([B,H,N,d]) is given, D_i = sum_c dO_ic o_ic instead: the backward as an operator of its
+    inputs (q, k, v, o, dO, LSE), the form the method's backward takes (equal to the first
+    when o is the exact forward output).  Rows whose LSE is -inf contribute nothing.  ``rows``
     restricts the computation to those query rows: dQ and D are filled for them only and dK,
     dV hold only their contributions (a sample of the work, used for timing).
     """
@@ -172,7 +175,10 @@ def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, bloc
                 s = _scores(q[b, h, r], k[b, h, cols], scale, ok)
                 p = _probs(s, _row_lse(s))
                 dp = do[b, h, r] @ v[b, h, cols].T
-                D = (p * dp).sum(axis=1)
+                if o is None:
+                    D = (p * dp).sum(axis=1)
+                else:
+                    D = (do[b, h, r] * np.asarray(o, dtype=np.float64)[b, h, r]).sum(axis=1)
                 ds = p * (dp - D[:, None])
                 dQ[b, hi, r] = scale * (ds @ k[b, h, cols])
                 dK[b, hi, cols] += scale * (ds.T @ q[b, h, r])

@@ -16,9 +16,8 @@ OK, INVALID, UNSUPPORTED = 0, 1, 2
 
 @pytest.fixture(scope="module")
 def lib():
-    if not os.path.exists(LIB):
-        import __graft_entry__
-        __graft_entry__.build()
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     L = ctypes.CDLL(LIB)
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.fa_forward.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp, vp]
@@ -74,6 +73,8 @@ def test_forward_argument_checks(lib):
     assert fwd(lib, N=-5) == INVALID
     assert fwd(lib, scale=float("nan")) == INVALID
     assert fwd(lib, scale=float("inf")) == INVALID
+    assert fwd(lib, scale=0.0) == INVALID
+    assert fwd(lib, scale=-0.5) == INVALID
     assert fwd(lib, q=None) == INVALID
     assert fwd(lib, lse=None) == INVALID
     assert fwd(lib, v=MIS) == INVALID

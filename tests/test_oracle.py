@@ -358,3 +358,24 @@ def test_backward_row_samples_add_up():
     assert np.max(np.abs(b[0][:, :, 61:] - full[0][:, :, 61:])) < 1e-13
     for i in (1, 2):
         assert np.max(np.abs(a[i] + b[i] - full[i])) < 1e-12
+
+
+def test_backward_with_given_output():
+    """Given the exact forward output, D = rowsum(dO * O) reproduces the exact gradient; given a
+    perturbed output, only the D term changes: dV is unchanged and dQ moves by the closed form
+    -scale * (dD_i) * sum_j P_ij k_j."""
+    B, H, N, d, scale = 1, 2, 90, 5, 0.45
+    q, k, v, do = (_rand((B, H, N, d), s) for s in (56, 57, 58, 59))
+    O, _ = oracle.forward(q, k, v, scale, causal=True)
+    ref = oracle.backward(q, k, v, do, scale, causal=True)
+    got = oracle.backward(q, k, v, do, scale, causal=True, o=O)
+    for a, b in zip(got, ref):
+        assert np.max(np.abs(a - b)) < 1e-12
+    Op = O + 1e-3 * _rand(O.shape, 60)
+    pert = oracle.backward(q, k, v, do, scale, causal=True, o=Op)
+    assert np.max(np.abs(pert[2] - ref[2])) < 1e-13
+    dD = (do * (Op - O)).sum(-1)
+    for h in range(H):
+        P = oracle.probabilities(q[0, h], k[0, h], scale, causal=True)
+        expect = ref[0][0, h] - scale * dD[0, h][:, None] * (P @ k[0, h])
+        assert np.max(np.abs(pert[0][0, h] - expect)) < 1e-12

@@ -25,6 +25,8 @@ MUTATIONS = [
      "lse = m0 + np.log2(np.exp(s - m0[:, None]).sum(axis=1))"),
     ("O[b, hi, c0:c0 + r.size] = p @ v[b, h, cols]", "O[b, hi, c0:c0 + r.size] = p @ v[b, h, cols[::-1]]"),
     ("shrink = np.exp(run_max - new_max)", "shrink = np.exp(new_max - run_max)"),
+    ("D = (do[b, h, r] * np.asarray(o, dtype=np.float64)[b, h, r]).sum(axis=1)",
+     "D = (q[b, h, r] * np.asarray(o, dtype=np.float64)[b, h, r]).sum(axis=1)"),
     ("return m, fa * la + fb * lb, fa * np.asarray(ua) + fb * np.asarray(ub)",
      "return m, fa * la + fb * lb, fa * np.asarray(ua) + fa * np.asarray(ub)"),
 ]

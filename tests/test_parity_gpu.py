@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import compare, f64, run_gpu
+from gpu_helpers import check_backward_given_o, compare, compare_fwd, f64, run_gpu
 from workloads import WORKLOADS, Workload, make_inputs, random_tile_mask
 
 pytestmark = pytest.mark.gpu
@@ -32,6 +32,7 @@ def test_fp32_workload_n128_d64():
 def test_fp32_shapes(N, d, causal):
     x = _case(N, d, "fp32", causal, B=1, H=2, seed=N)
     compare(x, run_gpu(x))
+    check_backward_given_o(x)
 
 
 # --- bf16 path: shapes, tails, masks ---------------------------------------------------------
@@ -41,7 +42,8 @@ def test_fp32_shapes(N, d, causal):
 @pytest.mark.parametrize("causal", [False, True])
 def test_bf16_shapes(N, d, causal):
     x = _case(N, d, "bf16", causal, seed=N * 7 + d + causal)
-    compare(x, run_gpu(x))
+    compare_fwd(x, run_gpu(x, backward=False))
+    check_backward_given_o(x)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -49,7 +51,8 @@ def test_bf16_shapes(N, d, causal):
 def test_bf16_key_padding(d, causal):
     x = _case(600, d, "bf16", causal, B=4, H=2, pad=(1, 600), seed=11 + d)
     x["kv_lens"] = torch.tensor([0, 1, 333, 600], dtype=torch.int32)   # includes an empty sequence
-    compare(x, run_gpu(x))
+    compare_fwd(x, run_gpu(x, backward=False))
+    check_backward_given_o(x)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -63,7 +66,8 @@ def test_bf16_random_tile_mask(d, causal, density):
         bm[:, 0] = 1
         bm[3, 0] = 0
     x["block_mask"] = bm
-    compare(x, run_gpu(x))
+    compare_fwd(x, run_gpu(x, backward=False))
+    check_backward_given_o(x)
 
 
 def test_bf16_mask_combination():
@@ -72,6 +76,7 @@ def test_bf16_mask_combination():
     x["block_mask"] = random_tile_mask(8, 0.5, seed=3)
     x["block_mask"][torch.arange(8), torch.arange(8)] = 1
     compare(x, run_gpu(x))
+    check_backward_given_o(x)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -83,7 +88,8 @@ def test_bf16_extreme_logits(d):
     out = run_gpu(x)
     for t in out.values():
         assert torch.isfinite(t).all()
-    compare(x, out)
+    compare_fwd(x, out)
+    check_backward_given_o(x)
 
 
 def test_empty_problem_is_noop():
