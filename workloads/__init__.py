@@ -52,6 +52,8 @@ WORKLOADS = {
     "long_n16k_d128": Workload("long_n16k_d128", 1, 16, 16384, 128, "bf16"),
     "long_n16k_d128_causal": Workload("long_n16k_d128_causal", 1, 16, 16384, 128, "bf16",
                                       causal=True),
+    # a smaller long-context case for profiler captures (inputs still larger than L2)
+    "long_n8k_d128": Workload("long_n8k_d128", 1, 16, 8192, 128, "bf16"),
     # block-sparse attention B1 H8 N65536 d64, local band + global tiles
     "block_sparse_n64k_d64": Workload("block_sparse_n64k_d64", 1, 8, 65536, 64, "bf16",
                                       block_sparse=True),
