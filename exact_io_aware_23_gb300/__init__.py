@@ -14,7 +14,7 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["forward", "backward", "backward_workspace_size", "check_device_status",
+__all__ = ["forward", "backward", "backward_noalloc", "backward_workspace_size", "check_device_status",
            "set_fault_injection", "set_wait_limit_ms", "FaError", "LIB_PATH", "lib"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
@@ -52,6 +52,11 @@ def _load() -> ctypes.CDLL:
     L.fa_debug_set_wait_limit_ms.restype = None
     L.fa_version.argtypes = []
     L.fa_version.restype = i
+    L.fa_backward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i,
+                                      vp, vp]
+    L.fa_backward_noalloc.restype = i
+    L.fa_backward_noalloc_max_workspace.argtypes = []
+    L.fa_backward_noalloc_max_workspace.restype = sz
     return L
 
 
@@ -153,3 +158,26 @@ def set_fault_injection(mode: int) -> None:
 
 def set_wait_limit_ms(ms: int) -> None:
     lib.fa_debug_set_wait_limit_ms(int(ms))
+
+
+def backward_noalloc(q, k, v, o, lse, do, *, causal: bool = False, scale: Optional[float] = None,
+                     block_mask=None, kv_lens=None, dq=None, dk=None, dv=None, stream=None):
+    """fa_backward_noalloc: the backward with the library's built-in scratch instead of a
+    workspace (for callers that cannot allocate device memory).  Output tensors may be passed
+    in so that the call itself allocates nothing."""
+    B, H, N, d = _check_qkv(q, k, v)
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = lib.fa_backward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, scale,
+                                 int(bool(causal)), _ptr(block_mask), _DTYPES[q.dtype],
+                                 _ptr(kv_lens), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_backward_noalloc")
+    return dq, dk, dv
+
+
+def noalloc_max_workspace() -> int:
+    return int(lib.fa_backward_noalloc_max_workspace())

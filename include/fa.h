@@ -102,6 +102,28 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_backward without a caller workspace, for callers that cannot allocate device memory:
+ * plugin interfaces that pass only input and output pointers, hosts whose device memory is all
+ * reserved by their own allocator, and latency-critical paths where cudaMalloc (which
+ * synchronises the device) is not allowed.  The pages have no counterpart of this call.
+ * The scratch comes from a fixed array of fa_backward_noalloc_max_workspace() bytes (32 MiB)
+ * built into the library; every GPU that loads the library holds it until the process exits.
+ * Arguments and results are those of fa_backward.  Returns FA_ERR_UNSUPPORTED, launching
+ * nothing, when fa_backward_workspace_size(B, H, N, d) exceeds that size.  The first call on a
+ * device looks up the array's device address; make it before any stream capture.  All calls
+ * share the array: calls that overlap on the GPU race on it and must be serialised.  Nothing
+ * carries over between calls (the dQ accumulator is zeroed by every call).
+ */
+fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o,
+                              const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, float scale, int causal,
+                              const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                              void* stream);
+
+/* Size in bytes of fa_backward_noalloc's built-in scratch array (no counterpart in the pages). */
+size_t fa_backward_noalloc_max_workspace(void);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error word.  Returns
  * FA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last check, FA_ERR_CUDA if
  * the synchronisation reported a CUDA error, FA_OK otherwise.
