@@ -16,8 +16,11 @@
 //               dV += P^T dO_i and dK += dS^T Q_i (TS: P^T, dS^T read from TMEM) and
 //               dQ_i = dS K_j (SS: dS staged in shared memory), two N = d/2 halves.
 //   warps 0-7   two warpgroups, query columns [0,64) and [64,128): P^T and dS^T in registers,
-//               written back to TMEM as bf16 and dS also to shared memory; then they add the
-//               tile's dQ into the fp32 workspace with vector atomics.
+//               written back to TMEM as bf16 and dS also to shared memory.  Then each warp
+//               copies its 32 rows of the tile's dQ (its warpgroup's half of d) from TMEM into
+//               the tile's Q/dO stage, which no MMA reads any more, and the TMA unit adds them
+//               into the fp32 workspace (bulk tensor reduce-add); the stage is handed back to
+//               the producer once the TMA unit has read it.
 //   TMEM d=128: dV [0,128) dK [128,256) X=S^T [256,384) Y=dP^T [384,512); P^T packed in
 //               X[0,64), dS^T packed in Y[0,64), dQ halves in X[64,128) and Y[64,128).
 //   TMEM d=64:  dV [0,64) dK [64,128) X [128,256) Y [256,384) dQ [384,448).
@@ -96,7 +99,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                 BwdArgs a) {
+                 const __grid_constant__ CUtensorMap tmDQ, BwdArgs a) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -126,7 +129,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     ptx::mbar_init(ptx::smem_u32(&bars->kv_full), 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->st_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->st_empty[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->st_empty[s]), 8);
     }
     ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
@@ -250,7 +253,6 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                           ptx::sdesc_sw128(kb + kk * 2048, 128 * 128, 1024), C::kIdescDQ, kk > 0);
           }
           ptx::mma_commit(ptx::smem_u32(&bars->dq_full));
-          ptx::mma_commit(ptx::smem_u32(&bars->st_empty[st]));
         }
       }
       ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
@@ -348,32 +350,48 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_ready));
-      // dQ of this query tile: lane = query row; this warpgroup takes half of d
+      // dQ of this query tile: lane = query row; this warpgroup takes half of d, in boxes of 32
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->dq_full), n & 1, lim_ms, a.err);
       if (!ok) break;
       ptx::tc_fence_after();
       {
-        const int q = i * BM + kr;
+        constexpr int kBoxes = D / 64;                 // 32-column boxes per warp
         const uint32_t src = D == 128 ? (wg == 0 ? C::kX + 64 : C::kY + 64) : 384 + wg * 32;
-        float* dst = a.dq_acc + ((size_t)bh * a.N + q) * D + wg * (D / 2);
+        uint32_t dqv[kBoxes][32];
 #pragma unroll
-        for (int hc = 0; hc < D / 64; ++hc) {
-          uint32_t raw[32];
-          ptx::tmem_ld32(tmem + lane_off + src + hc * 32, raw);
-          ptx::tmem_wait_ld();
-          if (q < a.N) {
+        for (int bx = 0; bx < kBoxes; ++bx) ptx::tmem_ld32(tmem + lane_off + src + bx * 32, dqv[bx]);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->dq_free));   // TMEM dQ may be reused
+        // stage: 32 rows x 32 fp32 per box, 128-byte swizzled, inside this tile's Q/dO buffer
+        uint8_t* stage = smem + C::kQ0 + st * 2 * C::kTile;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              atomicAdd(reinterpret_cast<float4*>(dst + hc * 32 + e),
-                        make_float4(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1]),
-                                    __uint_as_float(raw[e + 2]), __uint_as_float(raw[e + 3])));
-          }
+        for (int bx = 0; bx < kBoxes; ++bx) {
+          uint8_t* box = stage + ((wg * kBoxes + bx) * 4 + sub) * 4096;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(box + lane * 128 + ((ch ^ (lane & 7)) << 4)) =
+                make_uint4(dqv[bx][4 * ch], dqv[bx][4 * ch + 1], dqv[bx][4 * ch + 2], dqv[bx][4 * ch + 3]);
         }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int row0 = i * BM + sub * 32;
+          if (row0 < a.N) {
+#pragma unroll
+            for (int bx = 0; bx < kBoxes; ++bx)
+              ptx::tma_reduce_add_3d(&tmDQ, ptx::smem_u32(stage + ((wg * kBoxes + bx) * 4 + sub) * 4096),
+                                     wg * (D / 2) + bx * 32, row0, bh);
+            ptx::bulk_commit();
+            ptx::bulk_wait_read0();
+          }
+          ptx::mbar_arrive(ptx::smem_u32(&bars->st_empty[st]));            // stage back to producer
+        }
+        __syncwarp();
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->dq_free));
     }
+    if (lane == 0) ptx::bulk_wait0();                 // every reduction has landed in global memory
     // ------------------------------- epilogue: dV (warpgroup 0), dK (warpgroup 1) --------------
     const bool have = ok && n > 0;
     if (have) {
@@ -425,18 +443,28 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH) {
 
 template <int D>
 cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   const int BH = a.B * a.H;
   cudaError_t e;
   if ((e = make_map(&mq, a.q, D, a.N, BH)) != cudaSuccess) return e;
   if ((e = make_map(&mk, a.k, D, a.N, BH)) != cudaSuccess) return e;
   if ((e = make_map(&mv, a.v, D, a.N, BH)) != cudaSuccess) return e;
   if ((e = make_map(&mdo, a.dO, D, a.N, BH)) != cudaSuccess) return e;
+  {
+    // fp32 dQ workspace viewed as (d, N, B*H); boxes of 32 columns x 32 rows
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.N, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)a.N * D * 4};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if ((e = encode_tensor_map(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.dq_acc, dims, strides, box,
+                               estr, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+      return e;
+  }
   auto kern = bwd_sm103_kernel<D>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.N + BN - 1) / BN, a.H, a.B);
-  kern<<<grid, kThreads, Cfg<D>::kSmem, s>>>(mq, mk, mv, mdo, a);
+  kern<<<grid, kThreads, Cfg<D>::kSmem, s>>>(mq, mk, mv, mdo, mdq, a);
   return cudaGetLastError();
 }
 

@@ -149,7 +149,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const uint32_t tmem = bars->tmem_base;
 
   if (warp >= 8) {
-    ptx::regs_dec<56>();
+    ptx::regs_dec<88>();
     if (warp == 8 && lane == 0) {
       // ------------------------------- TMA producer -------------------------------------------
       ptx::tma_prefetch_desc(&tmQ);
@@ -255,7 +255,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
   } else {
     // ------------------------------- softmax warpgroups -----------------------------------------
-    ptx::regs_inc<208>();
+    ptx::regs_inc<200>();
     const int t = warp / 4;
     const int sub = warp % 4;
     const int r = sub * 32 + lane;                  // TMEM lane == row within the Q tile
@@ -403,11 +403,11 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   auto kern = fwd_sm103_kernel<D>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
   if (e != cudaSuccess) return e;
-  // The warp groups re-split the CTA's registers (4 warps down to 56, 8 warps up to 208 per
+  // The warp groups re-split the CTA's registers (4 warps down to 88, 8 warps up to 200 per
   // thread); that only completes if the launch holds at least that many registers.
   cudaFuncAttributes fattr;
   if ((e = cudaFuncGetAttributes(&fattr, kern)) != cudaSuccess) return e;
-  if (fattr.numRegs * kThreads < 128 * 56 + 256 * 208) return cudaErrorInvalidConfiguration;
+  if (fattr.numRegs * kThreads < 128 * 88 + 256 * 200) return cudaErrorInvalidConfiguration;
   dim3 grid((a.N + 2 * BM - 1) / (2 * BM), a.H, a.B);
   kern<<<grid, kThreads, Cfg<D>::kSmem, s>>>(mq, mk, mv, a);
   return cudaGetLastError();
