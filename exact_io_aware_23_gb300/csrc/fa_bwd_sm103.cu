@@ -12,9 +12,10 @@
 // one thread owns one key row of S^T, dP^T, P^T and dS^T:
 //   warp 8      TMA producer: K_j, V_j once; Q_i, dO_i through a two-stage ring, with the
 //               tile's LSE (as a log2-domain bias) and D vectors staged beside them.
-//   warp 9      MMA issuer: S^T = K_j Q_i^T and dP^T = V_j dO_i^T (SS), then
-//               dV += P^T dO_i and dK += dS^T Q_i (TS: P^T, dS^T read from TMEM) and
-//               dQ_i = dS K_j (SS: dS staged in shared memory), two N = d/2 halves.
+//   warp 9      MMA issuer: S^T = K_j Q_i^T and dP^T = V_j dO_i^T (SS); dV += P^T dO_i as
+//               soon as P^T is back in TMEM (overlapping the dS^T work), then dK += dS^T Q_i
+//               (TS: P^T, dS^T read from TMEM) and dQ_i = dS K_j (SS: dS staged in shared
+//               memory) in N = 64 parts.
 //   warps 0-7   two warpgroups, query columns [0,64) and [64,128): P^T and dS^T in registers,
 //               written back to TMEM as bf16 and dS also to shared memory.  Then each warp
 //               copies its 32 rows of the tile's dQ (its warpgroup's half of d) from TMEM into
@@ -68,6 +69,7 @@ struct Bars {
   uint64_t dp_full;
   uint64_t s_read;
   uint64_t dp_read;
+  uint64_t p_ready;
   uint64_t ds_ready;
   uint64_t dq_full;
   uint64_t dq_free;
@@ -135,6 +137,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->s_read), 8);
     ptx::mbar_init(ptx::smem_u32(&bars->dp_read), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->p_ready), 8);
     ptx::mbar_init(ptx::smem_u32(&bars->ds_ready), 8);
     ptx::mbar_init(ptx::smem_u32(&bars->dq_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->dq_free), 8);
@@ -226,21 +229,28 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                         ptx::sdesc_sw128(sdo + off, 16, 1024), C::kIdescST, kk > 0);
           }
           ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
+          // dV += P^T dO as soon as P^T is in TMEM (the dS^T work overlaps it).  A from TMEM: 16
+          // queries = 8 packed columns per step; B = dO with the query index as K (MN-major,
+          // 16 rows = 2048 bytes per step).
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_ready), n & 1, lim_ms, a.err);
+          if (!ok) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)
+            ptx::mma_ts(tmem + C::kDV, tmem + C::kX + kk * 8,
+                        ptx::sdesc_sw128(sdo + kk * 2048, 128 * 128, 1024), C::kIdescAcc,
+                        (n > 0 || kk > 0) ? 1u : 0u);
+          // dK += dS^T Q once dS^T is ready
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_ready), n & 1, lim_ms, a.err);
           if (ok && n > 0 && D == 64)
             ok = ptx::mbar_wait(ptx::smem_u32(&bars->dq_free), (n - 1) & 1, lim_ms, a.err);
           if (!ok) break;
           ptx::tc_fence_after();
-          // dV += P^T dO, dK += dS^T Q: A from TMEM (16 queries = 8 packed columns per step),
-          // B = dO / Q with the query index as K (MN-major, 16 rows = 2048 bytes per step)
 #pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk) {
-            const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
-            ptx::mma_ts(tmem + C::kDV, tmem + C::kX + kk * 8,
-                        ptx::sdesc_sw128(sdo + kk * 2048, 128 * 128, 1024), C::kIdescAcc, acc);
+          for (int kk = 0; kk < BM / 16; ++kk)
             ptx::mma_ts(tmem + C::kDK, tmem + C::kY + kk * 8,
-                        ptx::sdesc_sw128(sq + kk * 2048, 128 * 128, 1024), C::kIdescAcc, acc);
-          }
+                        ptx::sdesc_sw128(sq + kk * 2048, 128 * 128, 1024), C::kIdescAcc,
+                        (n > 0 || kk > 0) ? 1u : 0u);
           // dQ_i = dS K_j, 64 columns of d per part: A = dS (queries x keys, query-major in
           // shared memory), B = K (keys x d, d-major); 16 keys = 2048 bytes per step.
 #pragma unroll
@@ -310,6 +320,10 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 32; ++e) pk[e] = ptx::pack_bf16(p[2 * e], p[2 * e + 1]);
         ptx::tmem_st32(tmem + lane_off + C::kX + wg * 32, pk);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_ready));
       }
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->dp_full), n & 1, lim_ms, a.err);
       if (!ok) break;
