@@ -23,7 +23,8 @@
 //               into the fp32 workspace (bulk tensor reduce-add); the stage is handed back to
 //               the producer once the TMA unit has read it.
 //   TMEM d=128: dV [0,128) dK [128,256) X=S^T [256,384) Y=dP^T [384,512); P^T packed in
-//               X[0,64), dS^T packed in Y[0,64), dQ halves in X[64,128) and Y[64,128).
+//               X[0,64), dS^T packed in Y[0,64); once dK has read dS^T, the two dQ halves go to
+//               Y[0,64) and Y[64,128), so the next tile's S^T (into X) overlaps the dQ drain.
 //   TMEM d=64:  dV [0,64) dK [64,128) X [128,256) Y [256,384) dQ [384,448).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -208,8 +209,6 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         for (int i = g.next(g.i_begin); i < g.i_end && ok; i = g.next(i + 1), ++n) {
           const int st = n & 1;
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->st_full[st]), (n >> 1) & 1, lim_ms, a.err);
-          if (ok && n > 0 && D == 128)   // X, Y hold the previous tile's dQ until it is drained
-            ok = ptx::mbar_wait(ptx::smem_u32(&bars->dq_free), (n - 1) & 1, lim_ms, a.err);
           if (!ok) break;
           ptx::tc_fence_after();
           const uint32_t sq = sbase + C::kQ0 + st * 2 * C::kTile;
@@ -222,6 +221,11 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                         ptx::sdesc_sw128(sq + off, 16, 1024), C::kIdescST, kk > 0);
           }
           ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+          if (n > 0 && D == 128) {     // Y holds the previous tile's dQ until it is drained
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->dq_free), (n - 1) & 1, lim_ms, a.err);
+            if (!ok) break;
+            ptx::tc_fence_after();
+          }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
@@ -255,7 +259,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           // shared memory), B = K (keys x d, d-major); 16 keys = 2048 bytes per step.
 #pragma unroll
           for (int part = 0; part < C::kDQParts; ++part) {
-            const uint32_t dst = D == 128 ? (part == 0 ? C::kX + 64 : C::kY + 64) : 384;
+            const uint32_t dst = D == 128 ? C::kY + part * 64 : 384;
             const uint32_t kb = sbase + C::kK + part * 128 * 128;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
@@ -278,10 +282,16 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const bool key_ok = key < g.kv_lim;
     bool ok = true;
     int n = 0;
+    int pend_st = -1;                                // stage whose staged dQ is still being read
     for (int i = g.next(g.i_begin); i < g.i_end; i = g.next(i + 1), ++n) {
       const int st = n & 1;
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->st_full[st]), (n >> 1) & 1, lim_ms, a.err);
       if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full), n & 1, lim_ms, a.err);
+      if (lane == 0 && pend_st >= 0) {                // previous tile's staged dQ has been read
+        ptx::bulk_wait_read0();
+        ptx::mbar_arrive(ptx::smem_u32(&bars->st_empty[pend_st]));
+        pend_st = -1;
+      }
       if (!ok) break;
       ptx::tc_fence_after();
       const float* lse2 = reinterpret_cast<const float*>(smem + C::kVec + st * 1024) + wg * 64;
@@ -291,15 +301,17 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       // P^T for this thread's key row over 64 query columns
       float p[64];
       {
-        uint32_t raw[32];
+        uint32_t raw[2][32];
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) ptx::tmem_ld32(tmem + lane_off + C::kX + wg * 64 + hc * 32, raw[hc]);
+        ptx::tmem_wait_ld();
 #pragma unroll
         for (int hc = 0; hc < 2; ++hc) {
-          ptx::tmem_ld32(tmem + lane_off + C::kX + wg * 64 + hc * 32, raw);
-          ptx::tmem_wait_ld();
+          ptx::reg_fence(raw[hc]);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int col = hc * 32 + e;
-            float v = ptx::ex2(fmaf(__uint_as_float(raw[e]), c, -lse2[col]));
+            float v = ptx::ex2(fmaf(__uint_as_float(raw[hc][e]), c, -lse2[col]));
             if (kind == kPartial) {
               const bool allowed = key_ok && (!g.causal || key <= q0 + col);
               v = allowed ? v : 0.f;
@@ -329,15 +341,19 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (!ok) break;
       ptx::tc_fence_after();
       // dS^T = P^T * (dP^T - D)
+      {
+        uint32_t raw[2][32];
 #pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        uint32_t raw[32];
-        ptx::tmem_ld32(tmem + lane_off + C::kY + wg * 64 + hc * 32, raw);
+        for (int hc = 0; hc < 2; ++hc) ptx::tmem_ld32(tmem + lane_off + C::kY + wg * 64 + hc * 32, raw[hc]);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = hc * 32 + e;
-          p[col] = p[col] * (__uint_as_float(raw[e]) - dl[col]);
+        for (int hc = 0; hc < 2; ++hc) {
+          ptx::reg_fence(raw[hc]);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = hc * 32 + e;
+            p[col] = p[col] * (__uint_as_float(raw[hc][e]) - dl[col]);
+          }
         }
       }
       ptx::tc_fence_before();                         // all of dP^T read before dS^T overwrites Y
@@ -370,11 +386,13 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       ptx::tc_fence_after();
       {
         constexpr int kBoxes = D / 64;                 // 32-column boxes per warp
-        const uint32_t src = D == 128 ? (wg == 0 ? C::kX + 64 : C::kY + 64) : 384 + wg * 32;
+        const uint32_t src = D == 128 ? C::kY + wg * 64 : 384 + wg * 32;
         uint32_t dqv[kBoxes][32];
 #pragma unroll
         for (int bx = 0; bx < kBoxes; ++bx) ptx::tmem_ld32(tmem + lane_off + src + bx * 32, dqv[bx]);
         ptx::tmem_wait_ld();
+#pragma unroll
+        for (int bx = 0; bx < kBoxes; ++bx) ptx::reg_fence(dqv[bx]);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->dq_free));   // TMEM dQ may be reused
@@ -398,14 +416,16 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               ptx::tma_reduce_add_3d(&tmDQ, ptx::smem_u32(stage + ((wg * kBoxes + bx) * 4 + sub) * 4096),
                                      wg * (D / 2) + bx * 32, row0, bh);
             ptx::bulk_commit();
-            ptx::bulk_wait_read0();
           }
-          ptx::mbar_arrive(ptx::smem_u32(&bars->st_empty[st]));            // stage back to producer
+          pend_st = st;   // handed back to the producer once the TMA unit has read it
         }
         __syncwarp();
       }
     }
-    if (lane == 0) ptx::bulk_wait0();                 // every reduction has landed in global memory
+    if (lane == 0) {
+      ptx::bulk_wait0();                              // every reduction has landed in global memory
+      if (pend_st >= 0) ptx::mbar_arrive(ptx::smem_u32(&bars->st_empty[pend_st]));
+    }
     // ------------------------------- epilogue: dV (warpgroup 0), dK (warpgroup 1) --------------
     const bool have = ok && n > 0;
     if (have) {
@@ -421,6 +441,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (have && ok) {
         ptx::tmem_ld32(tmem + lane_off + src + hc * 32, raw);
         ptx::tmem_wait_ld();
+        ptx::reg_fence(raw);
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e) raw[e] = 0u;

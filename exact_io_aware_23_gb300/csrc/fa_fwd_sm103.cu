@@ -283,13 +283,15 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       } else {
         float s[BN];
         {
-          uint32_t raw[32];
+          uint32_t raw[4][32];                       // all 128 scores, one wait
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) ptx::tmem_ld32(tS + q4 * 32, raw[q4]);
+          ptx::tmem_wait_ld();
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
-            ptx::tmem_ld32(tS + q4 * 32, raw);
-            ptx::tmem_wait_ld();
+            ptx::reg_fence(raw[q4]);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) s[q4 * 32 + e] = __uint_as_float(raw[e]);
+            for (int e = 0; e < 32; ++e) s[q4 * 32 + e] = __uint_as_float(raw[q4][e]);
           }
         }
         if (kind == kPartial) {
@@ -297,9 +299,13 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
           for (int e = 0; e < BN; ++e) s[e] = e < lim ? s[e] : -INFINITY;
         }
-        float mx = s[0];
+        float m8[8];                                 // 8 independent chains, then a tree
 #pragma unroll
-        for (int e = 1; e < BN; ++e) mx = fmaxf(mx, s[e]);
+        for (int e = 0; e < 8; ++e) m8[e] = s[e];
+#pragma unroll
+        for (int e = 8; e < BN; ++e) m8[e & 7] = fmaxf(m8[e & 7], s[e]);
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         const float m_cand = mx * c;
         const bool need = m_cand > m_run + kRescaleLog2;   // false when the row is still empty
         const float alpha = need ? ptx::ex2(m_run - m_cand) : 1.f;
@@ -311,6 +317,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             uint32_t o[32];
             ptx::tmem_ld32(tO + q4 * 32, o);
             ptx::tmem_wait_ld();
+            ptx::reg_fence(o);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
             ptx::tmem_st32(tO + q4 * 32, o);
@@ -321,19 +328,19 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           m_run = m_cand;
         }
         const float msub = m_run == -INFINITY ? 0.f : m_run;
-        float lsum = 0.f;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};          // 4 independent partial sums
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const float p0 = ptx::ex2(fmaf(s[half * 64 + 2 * e], c, -msub));
             const float p1 = ptx::ex2(fmaf(s[half * 64 + 2 * e + 1], c, -msub));
-            lsum += p0 + p1;
+            ls[e & 3] += p0 + p1;
             pk[e] = ptx::pack_bf16(p0, p1);
           }
           ptx::tmem_st32(tS + half * 32, pk);
         }
-        l_run += lsum;
+        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -355,6 +362,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (have_o && ok) {
         ptx::tmem_ld32(tO + q4 * 32, o);
         ptx::tmem_wait_ld();
+        ptx::reg_fence(o);
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = 0u;
