@@ -173,13 +173,13 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (lane == 0) ok = ptx::mbar_wait(ptx::smem_u32(&bars->st_empty[st]), ph ^ 1, lim_ms, a.err);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        // LSE (as a log2-domain bias; +inf where P must vanish) and D for the tile's rows
+        // -LSE (as a log2-domain bias; -inf where P must vanish) and D for the tile's rows
         float* lse2 = reinterpret_cast<float*>(smem + C::kVec + st * 1024);
         float* dl = lse2 + 128;
         for (int r = lane; r < 128; r += 32) {
           const int q = i * BM + r;
           float L = q < a.N ? a.lse[(size_t)bh * a.N + q] : -INFINITY;
-          lse2[r] = L == -INFINITY ? INFINITY : L * kLog2e;
+          lse2[r] = L == -INFINITY ? -INFINITY : -L * kLog2e;   // stored negated
           dl[r] = q < a.N ? a.delta[(size_t)bh * a.N + q] : 0.f;
         }
         __syncwarp();
@@ -279,6 +279,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int key = g.k0 + kr;
     const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
     const float c = a.scale * kLog2e;
+    const float2 c2 = make_float2(c, c);
     const bool key_ok = key < g.kv_lim;
     bool ok = true;
     int n = 0;
@@ -287,11 +288,6 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const int st = n & 1;
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->st_full[st]), (n >> 1) & 1, lim_ms, a.err);
       if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full), n & 1, lim_ms, a.err);
-      if (lane == 0 && pend_st >= 0) {                // previous tile's staged dQ has been read
-        ptx::bulk_wait_read0();
-        ptx::mbar_arrive(ptx::smem_u32(&bars->st_empty[pend_st]));
-        pend_st = -1;
-      }
       if (!ok) break;
       ptx::tc_fence_after();
       const float* lse2 = reinterpret_cast<const float*>(smem + C::kVec + st * 1024) + wg * 64;
@@ -309,14 +305,18 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         for (int hc = 0; hc < 2; ++hc) {
           ptx::reg_fence(raw[hc]);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
+          for (int e = 0; e < 32; e += 2) {        // column pairs: packed fp32 arithmetic
             const int col = hc * 32 + e;
-            float v = ptx::ex2(fmaf(__uint_as_float(raw[hc][e]), c, -lse2[col]));
+            const float2 nl = *reinterpret_cast<const float2*>(lse2 + col);
+            const float2 x = ptx::fma2(make_float2(__uint_as_float(raw[hc][e]), __uint_as_float(raw[hc][e + 1])),
+                                       c2, nl);
+            float v0 = ptx::ex2(x.x), v1 = ptx::ex2(x.y);
             if (kind == kPartial) {
-              const bool allowed = key_ok && (!g.causal || key <= q0 + col);
-              v = allowed ? v : 0.f;
+              v0 = (key_ok && (!g.causal || key <= q0 + col)) ? v0 : 0.f;
+              v1 = (key_ok && (!g.causal || key <= q0 + col + 1)) ? v1 : 0.f;
             }
-            p[col] = v;
+            p[col] = v0;
+            p[col + 1] = v1;
           }
         }
       }
@@ -336,6 +336,12 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_ready));
+        if (lane == 0 && pend_st >= 0) {              // previous tile's staged dQ has been read
+          ptx::bulk_wait_read0();
+          ptx::mbar_arrive(ptx::smem_u32(&bars->st_empty[pend_st]));
+          pend_st = -1;
+        }
+        __syncwarp();
       }
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->dp_full), n & 1, lim_ms, a.err);
       if (!ok) break;
@@ -350,9 +356,13 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         for (int hc = 0; hc < 2; ++hc) {
           ptx::reg_fence(raw[hc]);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
+          for (int e = 0; e < 32; e += 2) {
             const int col = hc * 32 + e;
-            p[col] = p[col] * (__uint_as_float(raw[hc][e]) - dl[col]);
+            const float2 dd = ptx::sub2(make_float2(__uint_as_float(raw[hc][e]), __uint_as_float(raw[hc][e + 1])),
+                                        *reinterpret_cast<const float2*>(dl + col));
+            const float2 ds = ptx::mul2(make_float2(p[col], p[col + 1]), dd);
+            p[col] = ds.x;
+            p[col + 1] = ds.y;
           }
         }
       }

@@ -299,13 +299,13 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
           for (int e = 0; e < BN; ++e) s[e] = e < lim ? s[e] : -INFINITY;
         }
-        float m8[8];                                 // 8 independent chains, then a tree
+        float m8[8];                                 // 8 independent 3-input-max chains
 #pragma unroll
-        for (int e = 0; e < 8; ++e) m8[e] = s[e];
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(s[2 * k], s[2 * k + 1]);
 #pragma unroll
-        for (int e = 8; e < BN; ++e) m8[e & 7] = fmaxf(m8[e & 7], s[e]);
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int q = 8; q < BN / 2; ++q) m8[q & 7] = ptx::max3(m8[q & 7], s[2 * q], s[2 * q + 1]);
+        const float mx = ptx::max3(ptx::max3(m8[0], m8[1], m8[2]), ptx::max3(m8[3], m8[4], m8[5]),
+                                   fmaxf(m8[6], m8[7]));
         const float m_cand = mx * c;
         const bool need = m_cand > m_run + kRescaleLog2;   // false when the row is still empty
         const float alpha = need ? ptx::ex2(m_run - m_cand) : 1.f;
@@ -328,19 +328,23 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           m_run = m_cand;
         }
         const float msub = m_run == -INFINITY ? 0.f : m_run;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};          // 4 independent partial sums
+        // p = exp2(s*c - m) on column pairs; 4 independent packed partial sums
+        const float2 c2 = make_float2(c, c), nm2 = make_float2(-msub, -msub);
+        float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float p0 = ptx::ex2(fmaf(s[half * 64 + 2 * e], c, -msub));
-            const float p1 = ptx::ex2(fmaf(s[half * 64 + 2 * e + 1], c, -msub));
-            ls[e & 3] += p0 + p1;
-            pk[e] = ptx::pack_bf16(p0, p1);
+            const float2 x = ptx::fma2(make_float2(s[half * 64 + 2 * e], s[half * 64 + 2 * e + 1]), c2, nm2);
+            const float2 pp = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+            ls[e & 3] = ptx::add2(ls[e & 3], pp);
+            pk[e] = ptx::pack_bf16(pp.x, pp.y);
           }
           ptx::tmem_st32(tS + half * 32, pk);
         }
-        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        const float2 lsum = ptx::add2(ptx::add2(ls[0], ls[1]), ptx::add2(ls[2], ls[3]));
+        l_run += lsum.x + lsum.y;
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
