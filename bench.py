@@ -163,6 +163,17 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(values, device, world):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the job's time)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def workload_config(w):
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
             "key_padding": w.pad_lengths is not None, "block_sparse": w.block_sparse,
@@ -258,10 +269,7 @@ def run_ours(args, w):
     barrier()
     e2e_ms = s2.elapsed_time(e2)
 
-    times = torch.tensor([total_ms, e2e_ms, t_fwd, t_bwd], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms, t_fwd, t_bwd = times.tolist()
+    total_ms, e2e_ms, t_fwd, t_bwd = max_over_ranks([total_ms, e2e_ms, t_fwd, t_bwd], dev, world)
 
     F = forward_flops(w, B, H, N, x["block_mask"])
     ms_step = total_ms / args.steps

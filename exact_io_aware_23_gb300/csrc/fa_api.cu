@@ -39,6 +39,8 @@ fa_status check_common(int B, int H, int N, int d, float scale, fa_dtype dtype) 
   if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (H > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
+  // one CTA per (b, h, 128-row tile) must fit a 1-D grid
+  if ((size_t)B * (size_t)H * (size_t)((N + 127) / 128) > (size_t)0x7fffffff) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -87,6 +89,9 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
   a.B = B; a.H = H; a.N = N; a.d = d; a.scale = scale; a.causal = causal != 0;
   a.block_mask = block_mask; a.n_tiles = (N + fa::kMaskTile - 1) / fa::kMaskTile;
   a.kv_lens = kv_lens; a.dbg = knobs();
+  // Masks make the work per tile unequal: then every slice's heaviest tiles go first.  Without
+  // them, the tiles of one slice run together so its K/V (or Q/dO) stream is shared in L2.
+  a.heads_fastest = (a.causal || block_mask != nullptr || kv_lens != nullptr) ? 1 : 0;
   if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = dtype == FA_BF16 ? fa::launch_fwd_sm103(a, s) : fa::launch_fwd_simt(a, dtype, s);
@@ -123,6 +128,9 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   a.B = B; a.H = H; a.N = N; a.d = d; a.scale = scale; a.causal = causal != 0;
   a.block_mask = block_mask; a.n_tiles = (N + fa::kMaskTile - 1) / fa::kMaskTile;
   a.kv_lens = kv_lens; a.dbg = knobs();
+  // Masks make the work per tile unequal: then every slice's heaviest tiles go first.  Without
+  // them, the tiles of one slice run together so its K/V (or Q/dO) stream is shared in L2.
+  a.heads_fastest = (a.causal || block_mask != nullptr || kv_lens != nullptr) ? 1 : 0;
   if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = fa::launch_bwd_preprocess(a, dtype, s);

@@ -112,12 +112,18 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   }
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kBar);
   const uint32_t sbase = ptx::smem_u32(smem);
-  const int b = blockIdx.z, h = blockIdx.y;
-  const int bh = b * a.H + h;
+  // Work order.  With masks, the (b, h) slice varies fastest, so every slice's heaviest key
+  // tiles (the first ones when causal, the global columns of a block-sparse mask) run in the
+  // first waves.  Without, one slice's key tiles run together and share its Q/dO stream in L2.
+  const int BH = a.B * a.H;
+  const int n_kt = (a.N + BN - 1) / BN;
+  const int bh = a.heads_fastest ? (int)(blockIdx.x % BH) : (int)(blockIdx.x / n_kt);
+  const int jt = a.heads_fastest ? (int)(blockIdx.x / BH) : (int)(blockIdx.x % n_kt);   // key tile
+  const int b = bh / a.H;
   const uint32_t lim_ms = a.dbg.wait_limit_ms;
 
   Geo g;
-  g.k0 = blockIdx.x * BN;
+  g.k0 = jt * BN;
   g.N = a.N;
   int kvl = a.N;
   if (a.kv_lens != nullptr) kvl = max(0, min(a.N, (int)a.kv_lens[b]));
@@ -125,7 +131,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   g.causal = a.causal;
   g.T = a.n_tiles;
   g.bm = a.block_mask;
-  g.i_begin = a.causal ? blockIdx.x : 0;
+  g.i_begin = a.causal ? jt : 0;
   g.i_end = g.k0 < g.kv_lim ? (a.N + BM - 1) / BM : 0;
 
   if (threadIdx.x == 0) {
@@ -508,7 +514,7 @@ cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
   auto kern = bwd_sm103_kernel<D>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.N + BN - 1) / BN, a.H, a.B);
+  dim3 grid(((a.N + BN - 1) / BN) * BH);
   kern<<<grid, kThreads, Cfg<D>::kSmem, s>>>(mq, mk, mv, mdo, mdq, a);
   return cudaGetLastError();
 }

@@ -103,11 +103,15 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const uint32_t sKV = ptx::smem_u32(smem + C::kKVOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int b = blockIdx.z, h = blockIdx.y;
-  const int n_pairs = gridDim.x;
-  // heavier (later) query tiles first when causal
-  const int pair = a.causal ? n_pairs - 1 - blockIdx.x : blockIdx.x;
-  const int bh = b * a.H + h;
+  // Work order.  With masks, the (b, h) slice varies fastest, so every slice's heaviest Q-tile
+  // pair runs in the first waves (the last pairs when causal, the global rows of a block-sparse
+  // mask).  Without, one slice's pairs run together and share its K/V stream in L2.
+  const int BH = a.B * a.H;
+  const int n_pairs = (a.N + 2 * BM - 1) / (2 * BM);
+  const int bh = a.heads_fastest ? (int)(blockIdx.x % BH) : (int)(blockIdx.x / n_pairs);
+  const int slot = a.heads_fastest ? (int)(blockIdx.x / BH) : (int)(blockIdx.x % n_pairs);
+  const int pair = a.causal ? n_pairs - 1 - slot : slot;
+  const int b = bh / a.H;
 
   Geo g;
   g.q0 = pair * 2 * BM;
@@ -420,7 +424,7 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   cudaFuncAttributes fattr;
   if ((e = cudaFuncGetAttributes(&fattr, kern)) != cudaSuccess) return e;
   if (fattr.numRegs * kThreads < 128 * 88 + 256 * 200) return cudaErrorInvalidConfiguration;
-  dim3 grid((a.N + 2 * BM - 1) / (2 * BM), a.H, a.B);
+  dim3 grid(((a.N + 2 * BM - 1) / (2 * BM)) * BH);
   kern<<<grid, kThreads, Cfg<D>::kSmem, s>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }

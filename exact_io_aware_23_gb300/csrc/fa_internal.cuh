@@ -33,6 +33,7 @@ struct FwdArgs {
   const int32_t* kv_lens;     // [B] or null
   int* err;                   // device error word
   DebugKnobs dbg;
+  int heads_fastest;          // launch order: (b, h) slice fastest (unequal work per tile)
 };
 
 struct BwdArgs {
@@ -55,6 +56,7 @@ struct BwdArgs {
   const int32_t* kv_lens;
   int* err;
   DebugKnobs dbg;
+  int heads_fastest;          // launch order: (b, h) slice fastest (unequal work per tile)
 };
 
 // CUDA-core (SIMT) kernels: the fp32 path.
