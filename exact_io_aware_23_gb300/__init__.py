@@ -20,8 +20,8 @@ __all__ = ["forward", "backward", "backward_noalloc", "backward_workspace_size",
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
-FA_BF16, FA_FP32 = 0, 1
-_DTYPES = {torch.bfloat16: FA_BF16, torch.float32: FA_FP32}
+FA_BF16, FA_FP32, FA_FP16 = 0, 1, 2
+_DTYPES = {torch.bfloat16: FA_BF16, torch.float32: FA_FP32, torch.float16: FA_FP16}
 
 
 class FaError(RuntimeError):
@@ -102,7 +102,7 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool =
             scale: Optional[float] = None, block_mask: Optional[torch.Tensor] = None,
             kv_lens: Optional[torch.Tensor] = None, o: Optional[torch.Tensor] = None,
             lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """O, LSE = attention forward (fa_forward).  q, k, v: [B, H, N, d] bf16 or fp32 on CUDA."""
+    """O, LSE = attention forward (fa_forward).  q, k, v: [B, H, N, d] bf16, fp16 or fp32 on CUDA."""
     B, H, N, d = _check_qkv(q, k, v)
     scale = 1.0 / d ** 0.5 if scale is None else float(scale)
     block_mask, kv_lens = _masks(block_mask, kv_lens, B, N, q.device)

@@ -36,13 +36,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 fa_status check_common(int B, int H, int N, int d, float scale, fa_dtype dtype) {
   if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
   if (!isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_BF16 && dtype != FA_FP32 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (H > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
   // one CTA per (b, h, 128-row tile) must fit a 1-D grid
   if ((size_t)B * (size_t)H * (size_t)((N + 127) / 128) > (size_t)0x7fffffff) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
+
+// A block-sparse mask is kept as a one-bit-per-tile list in shared memory: N <= 786432.
+constexpr int kMaxBlockSparseN = 786432;
 
 fa::DebugKnobs knobs() {
   fa::DebugKnobs k;
@@ -81,6 +84,7 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
   fa_status st = check_common(B, H, N, d, scale, dtype);
   if (st != FA_OK) return st;
   if (B == 0 || H == 0 || N == 0) return FA_OK;
+  if (block_mask != nullptr && N > kMaxBlockSparseN) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
@@ -94,7 +98,7 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
   a.heads_fastest = (a.causal || block_mask != nullptr || kv_lens != nullptr) ? 1 : 0;
   if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = dtype == FA_BF16 ? fa::launch_fwd_sm103(a, s) : fa::launch_fwd_simt(a, dtype, s);
+  cudaError_t e = dtype == FA_FP32 ? fa::launch_fwd_simt(a, dtype, s) : fa::launch_fwd_sm103(a, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -112,6 +116,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   fa_status st = check_common(B, H, N, d, scale, dtype);
   if (st != FA_OK) return st;
   if (B == 0 || H == 0 || N == 0) return FA_OK;
+  if (block_mask != nullptr && N > kMaxBlockSparseN) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace)
     return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
@@ -135,7 +140,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = fa::launch_bwd_preprocess(a, dtype, s);
   if (e == cudaSuccess)
-    e = dtype == FA_BF16 ? fa::launch_bwd_sm103(a, s) : fa::launch_bwd_simt(a, dtype, s);
+    e = dtype == FA_FP32 ? fa::launch_bwd_simt(a, dtype, s) : fa::launch_bwd_sm103(a, dtype, s);
   if (e == cudaSuccess) e = fa::launch_bwd_dq_convert(a, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

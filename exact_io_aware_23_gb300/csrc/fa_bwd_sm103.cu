@@ -1,4 +1,4 @@
-// Tensor-core attention backward for sm_103a (bf16 in, fp32 accumulate), d in {64, 128}.
+// Tensor-core attention backward for sm_103a (bf16 or fp16 in, fp32 accumulate), d in {64, 128}.
 //
 // The method ("FlashAttention paper story", backward paragraph; "FlashAttention: Exact Attention
 // with Less GPU Memory", "Tiling, and paying arithmetic to avoid memory"): only the per-row
@@ -44,7 +44,7 @@ constexpr int kThreads = 320;
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+template <int D, bool F16>
 struct Cfg {
   static constexpr int kTile = 128 * D * 2;                  // one 128-row operand tile
   static constexpr int kK = 0;
@@ -56,13 +56,13 @@ struct Cfg {
   static constexpr int kSmem = kBar + 256;
   // TMEM columns
   static constexpr uint32_t kDV = 0, kDK = D, kX = 2 * D, kY = 2 * D + 128;
-  static constexpr uint32_t kIdescST = ptx::idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-  static constexpr uint32_t kIdescAcc = ptx::idesc_bf16_f32(128, D, false, true);    // dV, dK
-  static constexpr uint32_t kIdescDQ = ptx::idesc_bf16_f32(128, 64, true, true);     // dQ parts
+  static constexpr uint32_t kIdescST = ptx::idesc_f32acc(128, 128, false, false, F16);  // S^T, dP^T
+  static constexpr uint32_t kIdescAcc = ptx::idesc_f32acc(128, D, false, true, F16);    // dV, dK
+  static constexpr uint32_t kIdescDQ = ptx::idesc_f32acc(128, 64, true, true, F16);     // dQ parts
   static constexpr int kDQParts = D / 64;                    // N = 64 columns of d per part
 };
 
-struct Bars {
+struct Bars {             // at most 128 bytes (the live-tile bitmap follows)
   uint64_t kv_full;
   uint64_t st_full[2];
   uint64_t st_empty[2];
@@ -78,6 +78,8 @@ struct Bars {
   uint32_t tmem_base;
 };
 
+static_assert(sizeof(Bars) <= 128, "the live-tile bitmap starts 128 bytes after the barriers");
+
 enum : int { kNone = 0, kPartial = 1, kFull = 2 };
 
 struct Geo {
@@ -92,18 +94,27 @@ struct Geo {
     if (c1 < kv_lim && (!causal || c1 <= r0)) return kFull;
     return kPartial;
   }
+  // Without a tile mask the live query tiles are exactly [i_begin, i_end).  With one, `bits`
+  // (shared memory, built once per CTA) marks the live tiles and the next one is found a word
+  // at a time.
+  const uint32_t* bits;
   __device__ int next(int i) const {
-    while (i < i_end && kind(i) == kNone) ++i;
-    return i;
+    if (bits == nullptr) return i;
+    while (i < i_end) {
+      const uint32_t w = bits[i >> 5] >> (i & 31);
+      if (w != 0u) return min(i + __ffs(w) - 1, i_end);
+      i = (i | 31) + 1;
+    }
+    return i_end;
   }
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                  const __grid_constant__ CUtensorMap tmDQ, BwdArgs a) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F16>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if ((ptx::smem_u32(smem) & 1023u) != 0) {      // the operand tiles need 1 KB alignment
@@ -154,6 +165,16 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (warp == 9) {
     ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
     ptx::tmem_relinquish();
+  }
+  g.bits = nullptr;
+  if (a.block_mask != nullptr) {                 // live-tile bitmap, one ballot per 32 tiles
+    uint32_t* live_bits = reinterpret_cast<uint32_t*>(smem + C::kBar + 128);
+    g.bits = live_bits;
+    for (int w = warp; w < (g.i_end + 31) / 32; w += kThreads / 32) {
+      const int i = w * 32 + lane;
+      const uint32_t word = __ballot_sync(0xffffffffu, i >= g.i_begin && i < g.i_end && g.kind(i) != kNone);
+      if (lane == 0) live_bits[w] = word;
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -336,7 +357,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack_bf16(p[2 * e], p[2 * e + 1]);
+        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
         ptx::tmem_st32(tmem + lane_off + C::kX + wg * 32, pk);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -381,7 +402,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack_bf16(p[2 * e], p[2 * e + 1]);
+        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
         ptx::tmem_st32(tmem + lane_off + C::kY + wg * 32, pk);
         // dS into shared memory, query-major 128-byte-swizzled: row = key, 64 queries per atom
         uint8_t* row = smem + C::kDS + wg * (128 * 128) + kr * 128;
@@ -449,7 +470,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       ptx::tc_fence_after();
     }
     const float mult = wg == 0 ? 1.f : a.scale;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(wg == 0 ? a.dv : a.dk) + ((size_t)bh * a.N + key) * D;
+    uint16_t* out = static_cast<uint16_t*>(wg == 0 ? a.dv : a.dk) + ((size_t)bh * a.N + key) * D;
     const uint32_t src = wg == 0 ? C::kDV : C::kDK;
 #pragma unroll 1
     for (int hc = 0; hc < D / 32; ++hc) {
@@ -467,10 +488,10 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4) {
           uint4 w;
-          w.x = ptx::pack_bf16(__uint_as_float(raw[8 * v4 + 0]) * mult, __uint_as_float(raw[8 * v4 + 1]) * mult);
-          w.y = ptx::pack_bf16(__uint_as_float(raw[8 * v4 + 2]) * mult, __uint_as_float(raw[8 * v4 + 3]) * mult);
-          w.z = ptx::pack_bf16(__uint_as_float(raw[8 * v4 + 4]) * mult, __uint_as_float(raw[8 * v4 + 5]) * mult);
-          w.w = ptx::pack_bf16(__uint_as_float(raw[8 * v4 + 6]) * mult, __uint_as_float(raw[8 * v4 + 7]) * mult);
+          w.x = ptx::pack2<F16>(__uint_as_float(raw[8 * v4 + 0]) * mult, __uint_as_float(raw[8 * v4 + 1]) * mult);
+          w.y = ptx::pack2<F16>(__uint_as_float(raw[8 * v4 + 2]) * mult, __uint_as_float(raw[8 * v4 + 3]) * mult);
+          w.z = ptx::pack2<F16>(__uint_as_float(raw[8 * v4 + 4]) * mult, __uint_as_float(raw[8 * v4 + 5]) * mult);
+          w.w = ptx::pack2<F16>(__uint_as_float(raw[8 * v4 + 6]) * mult, __uint_as_float(raw[8 * v4 + 7]) * mult);
           dst[v4] = w;
         }
       }
@@ -483,24 +504,24 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (warp == 9) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
-cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH) {
+cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH, bool f16) {
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
   const cuuint32_t box[3] = {64, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+  return encode_tensor_map(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv, mdo, mdq;
   const int BH = a.B * a.H;
   cudaError_t e;
-  if ((e = make_map(&mq, a.q, D, a.N, BH)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, a.k, D, a.N, BH)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, a.v, D, a.N, BH)) != cudaSuccess) return e;
-  if ((e = make_map(&mdo, a.dO, D, a.N, BH)) != cudaSuccess) return e;
+  if ((e = make_map(&mq, a.q, D, a.N, BH, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, a.k, D, a.N, BH, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.v, D, a.N, BH, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mdo, a.dO, D, a.N, BH, F16)) != cudaSuccess) return e;
   {
     // fp32 dQ workspace viewed as (d, N, B*H); boxes of 32 columns x 32 rows
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.N, (cuuint64_t)BH};
@@ -511,18 +532,22 @@ cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
                                estr, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
       return e;
   }
-  auto kern = bwd_sm103_kernel<D>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
+  auto kern = bwd_sm103_kernel<D, F16>;
+  // barriers (128 bytes) + the live-tile bitmap of a block-sparse mask (one bit per query tile)
+  int smem = Cfg<D, F16>::kSmem;
+  if (a.block_mask != nullptr) smem = max(smem, Cfg<D, F16>::kBar + 128 + ((a.n_tiles + 127) / 128) * 16);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(((a.N + BN - 1) / BN) * BH);
-  kern<<<grid, kThreads, Cfg<D>::kSmem, s>>>(mq, mk, mv, mdo, mdq, a);
+  kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mdo, mdq, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_sm103(const BwdArgs& a, cudaStream_t s) {
-  return a.d == 64 ? launch<64>(a, s) : launch<128>(a, s);
+cudaError_t launch_bwd_sm103(const BwdArgs& a, fa_dtype dt, cudaStream_t s) {
+  if (dt == FA_FP16) return a.d == 64 ? launch<64, true>(a, s) : launch<128, true>(a, s);
+  return a.d == 64 ? launch<64, false>(a, s) : launch<128, false>(a, s);
 }
 
 }  // namespace fa

@@ -1,4 +1,4 @@
-// Tensor-core attention forward for sm_103a (bf16 in, fp32 accumulate), d in {64, 128}.
+// Tensor-core attention forward for sm_103a (bf16 or fp16 in, fp32 accumulate), d in {64, 128}.
 //
 // The method ("FlashAttention paper story", tiling and online-softmax paragraphs; "FlashAttention：
 // 让精确注意力服从内存层次", section "Online softmax" and its merge law): Q is cut into row
@@ -42,7 +42,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 enum : int { kNone = 0, kPartial = 1, kFull = 2 };
 
-template <int D>
+template <int D, bool F16>
 struct Cfg {
   static constexpr int kTileBytes = BN * D * 2;                 // one K or V tile; one Q tile
   static constexpr int kSlots = D == 128 ? 5 : 8;               // K/V ring depth
@@ -50,8 +50,8 @@ struct Cfg {
   static constexpr int kKVOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
   static constexpr int kSmem = kBarOff + 256 + 1024;            // + barriers + alignment slack
-  static constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(BM, BN, false, false);
-  static constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(BM, D, false, true);
+  static constexpr uint32_t kIdescS = ptx::idesc_f32acc(BM, BN, false, false, F16);
+  static constexpr uint32_t kIdescO = ptx::idesc_f32acc(BM, D, false, true, F16);
 };
 
 struct Bars {            // all mbarriers of one CTA (8 bytes each)
@@ -65,8 +65,11 @@ struct Bars {            // all mbarriers of one CTA (8 bytes each)
   uint32_t tmem_base;
 };
 
+static_assert(sizeof(Bars) <= 256, "the live-tile bitmap starts 256 bytes after the barriers");
+
 // Per-CTA tile geometry: which key tiles exist and how each Q tile must treat them.
 struct Geo {
+  int bh;          // (b, h) slice
   int q0;          // first query row of Q tile 0
   int N, kv_lim;   // keys with j >= kv_lim are masked (padding and tail)
   int causal;
@@ -85,17 +88,25 @@ struct Geo {
     return kPartial;
   }
   __device__ bool live(int j) const { return kind(0, j) != kNone || kind(1, j) != kNone; }
+  // Without a tile mask the live key tiles are exactly [0, j_end).  With one, `bits` (shared
+  // memory, built once per CTA) marks the live tiles and the next one is found a word at a time.
+  const uint32_t* bits;
   __device__ int next(int j) const {
-    while (j < j_end && !live(j)) ++j;
-    return j;
+    if (bits == nullptr) return j;
+    while (j < j_end) {
+      const uint32_t w = bits[j >> 5] >> (j & 31);
+      if (w != 0u) return min(j + __ffs(w) - 1, j_end);
+      j = (j | 31) + 1;
+    }
+    return j_end;
   }
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, FwdArgs a) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOff);
@@ -103,30 +114,35 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const uint32_t sKV = ptx::smem_u32(smem + C::kKVOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Work order.  With masks, the (b, h) slice varies fastest, so every slice's heaviest Q-tile
-  // pair runs in the first waves (the last pairs when causal, the global rows of a block-sparse
-  // mask).  Without, one slice's pairs run together and share its K/V stream in L2.
-  const int BH = a.B * a.H;
-  const int n_pairs = (a.N + 2 * BM - 1) / (2 * BM);
-  const int bh = a.heads_fastest ? (int)(blockIdx.x % BH) : (int)(blockIdx.x / n_pairs);
-  const int slot = a.heads_fastest ? (int)(blockIdx.x / BH) : (int)(blockIdx.x % n_pairs);
-  const int pair = a.causal ? n_pairs - 1 - slot : slot;
-  const int b = bh / a.H;
-
-  Geo g;
-  g.q0 = pair * 2 * BM;
-  g.N = a.N;
-  int kvl = a.N;
-  if (a.kv_lens != nullptr) kvl = max(0, min(a.N, (int)a.kv_lens[b]));
-  g.kv_lim = kvl;
-  g.causal = a.causal;
-  g.bm = a.block_mask;
-  g.T = a.n_tiles;
-  {
+  uint32_t* const live_bits = reinterpret_cast<uint32_t*>(smem + C::kBarOff + 256);
+  // Each role builds its own copy after its register reallocation (cheap integer work), so no
+  // value computed here has to survive, spilled, into the role loops.
+  auto make_geo = [&]() {
+    // Work order.  With masks, the (b, h) slice varies fastest, so every slice's heaviest Q-tile
+    // pair runs in the first waves (the last pairs when causal, the global rows of a
+    // block-sparse mask).  Without, one slice's pairs run together and share its K/V stream in L2.
+    const int BH = a.B * a.H;
+    const int n_pairs = (a.N + 2 * BM - 1) / (2 * BM);
+    const int bh = a.heads_fastest ? (int)(blockIdx.x % BH) : (int)(blockIdx.x / n_pairs);
+    const int slot = a.heads_fastest ? (int)(blockIdx.x / BH) : (int)(blockIdx.x % n_pairs);
+    const int pair = a.causal ? n_pairs - 1 - slot : slot;
+    const int b = bh / a.H;
+    Geo g;
+    g.bh = bh;
+    g.q0 = pair * 2 * BM;
+    g.N = a.N;
+    int kvl = a.N;
+    if (a.kv_lens != nullptr) kvl = max(0, min(a.N, (int)a.kv_lens[b]));
+    g.kv_lim = kvl;
+    g.causal = a.causal;
+    g.bm = a.block_mask;
+    g.T = a.n_tiles;
     int last_key = g.kv_lim;
     if (a.causal) last_key = min(last_key, min(g.q0 + 2 * BM, a.N));
     g.j_end = (last_key + BN - 1) / BN;
-  }
+    g.bits = a.block_mask != nullptr ? live_bits : nullptr;
+    return g;
+  };
   const uint32_t lim_ms = a.dbg.wait_limit_ms;
 
   if (threadIdx.x == 0) {
@@ -147,6 +163,16 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
     ptx::tmem_relinquish();
   }
+  if (a.block_mask != nullptr && warp == 10) {   // live-tile bitmap, one ballot per 32 tiles
+    const Geo g = make_geo();
+    {
+      for (int w = 0; w < (g.j_end + 31) / 32; ++w) {
+        const int j = w * 32 + lane;
+        const uint32_t word = __ballot_sync(0xffffffffu, j < g.j_end && g.live(j));
+        if (lane == 0) live_bits[w] = word;
+      }
+    }
+  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -154,6 +180,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
   if (warp >= 8) {
     ptx::regs_dec<88>();
+    const Geo g = make_geo();
+    const int bh = g.bh;
     if (warp == 8 && lane == 0) {
       // ------------------------------- TMA producer -------------------------------------------
       ptx::tma_prefetch_desc(&tmQ);
@@ -260,6 +288,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   } else {
     // ------------------------------- softmax warpgroups -----------------------------------------
     ptx::regs_inc<200>();
+    const Geo g = make_geo();
+    const int bh = g.bh;
     const int t = warp / 4;
     const int sub = warp % 4;
     const int r = sub * 32 + lane;                  // TMEM lane == row within the Q tile
@@ -343,7 +373,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             const float2 x = ptx::fma2(make_float2(s[half * 64 + 2 * e], s[half * 64 + 2 * e + 1]), c2, nm2);
             const float2 pp = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
             ls[e & 3] = ptx::add2(ls[e & 3], pp);
-            pk[e] = ptx::pack_bf16(pp.x, pp.y);
+            pk[e] = ptx::pack2<F16>(pp.x, pp.y);
           }
           ptx::tmem_st32(tS + half * 32, pk);
         }
@@ -363,7 +393,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
     const bool any = l_run > 0.f;
     const float inv = any ? 1.f / l_run : 0.f;
-    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) + ((size_t)bh * a.N + i) * D;
+    uint16_t* orow = static_cast<uint16_t*>(a.o) + ((size_t)bh * a.N + i) * D;
 #pragma unroll 1
     for (int q4 = 0; q4 < D / 32; ++q4) {
       uint32_t o[32];
@@ -380,10 +410,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4) {
           uint4 w;
-          w.x = ptx::pack_bf16(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
-          w.y = ptx::pack_bf16(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
-          w.z = ptx::pack_bf16(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
-          w.w = ptx::pack_bf16(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+          w.x = ptx::pack2<F16>(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+          w.y = ptx::pack2<F16>(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+          w.z = ptx::pack2<F16>(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+          w.w = ptx::pack2<F16>(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
           dst[v4] = w;
         }
       }
@@ -399,25 +429,27 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
 // ---- host side -----------------------------------------------------------------------------------
 
-cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH) {
+cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH, bool f16) {
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
   const cuuint32_t box[3] = {64, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+  return encode_tensor_map(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
   const int BH = a.B * a.H;
   cudaError_t e;
-  if ((e = make_map(&mq, a.q, D, a.N, BH)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, a.k, D, a.N, BH)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, a.v, D, a.N, BH)) != cudaSuccess) return e;
-  auto kern = fwd_sm103_kernel<D>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
+  if ((e = make_map(&mq, a.q, D, a.N, BH, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, a.k, D, a.N, BH, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.v, D, a.N, BH, F16)) != cudaSuccess) return e;
+  auto kern = fwd_sm103_kernel<D, F16>;
+  // + the live-tile bitmap of a block-sparse mask (one bit per key tile)
+  const int smem = Cfg<D, F16>::kSmem + (a.block_mask != nullptr ? ((a.n_tiles + 127) / 128) * 16 : 0);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // The warp groups re-split the CTA's registers (4 warps down to 88, 8 warps up to 200 per
   // thread); that only completes if the launch holds at least that many registers.
@@ -425,14 +457,15 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   if ((e = cudaFuncGetAttributes(&fattr, kern)) != cudaSuccess) return e;
   if (fattr.numRegs * kThreads < 128 * 88 + 256 * 200) return cudaErrorInvalidConfiguration;
   dim3 grid(((a.N + 2 * BM - 1) / (2 * BM)) * BH);
-  kern<<<grid, kThreads, Cfg<D>::kSmem, s>>>(mq, mk, mv, a);
+  kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_sm103(const FwdArgs& a, cudaStream_t s) {
-  return a.d == 64 ? launch<64>(a, s) : launch<128>(a, s);
+cudaError_t launch_fwd_sm103(const FwdArgs& a, fa_dtype dt, cudaStream_t s) {
+  if (dt == FA_FP16) return a.d == 64 ? launch<64, true>(a, s) : launch<128, true>(a, s);
+  return a.d == 64 ? launch<64, false>(a, s) : launch<128, false>(a, s);
 }
 
 }  // namespace fa

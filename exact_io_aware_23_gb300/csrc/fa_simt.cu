@@ -1,6 +1,6 @@
 // CUDA-core (SIMT) attention kernels: the fp32 path of the library, and the backward's
 // bandwidth-bound pieces shared with the tensor-core path (D = rowsum(dO * O) and the final
-// dQ conversion).
+// dQ conversion, for fp32, bf16 and fp16).
 //
 // Forward ("FlashAttention paper story", tiling and online-softmax paragraphs): one CTA per
 // 64-row query block; K/V stream through shared memory 64 keys at a time; every query row
@@ -13,6 +13,7 @@
 // and visits every query block that may attend to it, rebuilding P = exp(scale*S - LSE).  dQ
 // is reduced across key blocks with fp32 atomics into the workspace.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "fa_internal.cuh"
@@ -27,9 +28,11 @@ constexpr int kThreads = 256;  // 8 warps
 template <typename T> __device__ __forceinline__ float to_f(T x);
 template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <> __device__ __forceinline__ float to_f<__half>(__half x) { return __half2float(x); }
 template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <> __device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -366,22 +369,25 @@ cudaError_t conv_launch(const BwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_fwd_simt(const FwdArgs& a, fa_dtype dt, cudaStream_t s) {
-  if (dt == FA_FP32) return a.d == 64 ? fwd_launch<float, 64>(a, s) : fwd_launch<float, 128>(a, s);
-  return a.d == 64 ? fwd_launch<__nv_bfloat16, 64>(a, s) : fwd_launch<__nv_bfloat16, 128>(a, s);
+  if (dt != FA_FP32) return cudaErrorInvalidValue;     // 16-bit inputs run on the tensor cores
+  return a.d == 64 ? fwd_launch<float, 64>(a, s) : fwd_launch<float, 128>(a, s);
 }
 
 cudaError_t launch_bwd_simt(const BwdArgs& a, fa_dtype dt, cudaStream_t s) {
-  if (dt == FA_FP32) return a.d == 64 ? bwd_launch<float, 64>(a, s) : bwd_launch<float, 128>(a, s);
-  return a.d == 64 ? bwd_launch<__nv_bfloat16, 64>(a, s) : bwd_launch<__nv_bfloat16, 128>(a, s);
+  if (dt != FA_FP32) return cudaErrorInvalidValue;
+  return a.d == 64 ? bwd_launch<float, 64>(a, s) : bwd_launch<float, 128>(a, s);
 }
 
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, fa_dtype dt, cudaStream_t s) {
   if (dt == FA_FP32) return a.d == 64 ? pre_launch<float, 64>(a, s) : pre_launch<float, 128>(a, s);
+  if (dt == FA_FP16) return a.d == 64 ? pre_launch<__half, 64>(a, s) : pre_launch<__half, 128>(a, s);
   return a.d == 64 ? pre_launch<__nv_bfloat16, 64>(a, s) : pre_launch<__nv_bfloat16, 128>(a, s);
 }
 
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a, fa_dtype dt, cudaStream_t s) {
-  return dt == FA_FP32 ? conv_launch<float>(a, s) : conv_launch<__nv_bfloat16>(a, s);
+  if (dt == FA_FP32) return conv_launch<float>(a, s);
+  if (dt == FA_FP16) return conv_launch<__half>(a, s);
+  return conv_launch<__nv_bfloat16>(a, s);
 }
 
 }  // namespace fa

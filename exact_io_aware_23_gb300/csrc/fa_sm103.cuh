@@ -8,12 +8,12 @@
 
 namespace fa {
 
-// bf16 forward (tcgen05 + TMA), d in {64, 128}.
-cudaError_t launch_fwd_sm103(const FwdArgs& a, cudaStream_t s);
+// bf16 / fp16 forward (tcgen05 + TMA), d in {64, 128}.
+cudaError_t launch_fwd_sm103(const FwdArgs& a, fa_dtype dt, cudaStream_t s);
 
-// bf16 backward main kernel (tcgen05 + TMA), d in {64, 128}; runs between the preprocess and
-// the dQ conversion kernels.
-cudaError_t launch_bwd_sm103(const BwdArgs& a, cudaStream_t s);
+// bf16 / fp16 backward main kernel (tcgen05 + TMA), d in {64, 128}; runs between the
+// preprocess and the dQ conversion kernels.
+cudaError_t launch_bwd_sm103(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
 
 // Encodes a tiled TMA descriptor through the driver entry point (resolved once per process).
 cudaError_t encode_tensor_map(CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank,

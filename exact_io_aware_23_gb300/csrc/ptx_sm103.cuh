@@ -7,6 +7,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace fa {
@@ -146,12 +147,13 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, dense, no negation.
-// a_mn / b_mn select the MN-major (transposed) layout of the operand in shared memory.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
+// Instruction descriptor, kind::f16: A and B both bf16 (f16 = false) or both fp16 (f16 = true),
+// fp32 accumulator, dense, no negation.  a_mn / b_mn select the MN-major (transposed) layout of
+// the operand in shared memory.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool a_mn, bool b_mn, bool f16) {
   return (1u << 4)                           // accumulator format: F32
-         | (1u << 7)                         // A format: BF16
-         | (1u << 10)                        // B format: BF16
+         | ((f16 ? 0u : 1u) << 7)            // A format: F16 = 0, BF16 = 1
+         | ((f16 ? 0u : 1u) << 10)           // B format
          | ((a_mn ? 1u : 0u) << 15)          // A major-ness
          | ((b_mn ? 1u : 0u) << 16)          // B major-ness
          | ((uint32_t)(N >> 3) << 17)        // N / 8
@@ -279,6 +281,15 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// Two fp32 values rounded to the 16-bit operand type, lo in the low half.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
 }
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

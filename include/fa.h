@@ -56,7 +56,9 @@ typedef enum {
 
 typedef enum {
   FA_BF16 = 0,              /* bf16 inputs and outputs, fp32 accumulation (tcgen05 path) */
-  FA_FP32 = 1               /* fp32 inputs and outputs, fp32 CUDA-core arithmetic */
+  FA_FP32 = 1,              /* fp32 inputs and outputs, fp32 CUDA-core arithmetic */
+  FA_FP16 = 2               /* fp16 inputs and outputs, fp32 accumulation (tcgen05 path); P and
+                               dS enter the tensor cores as fp16, so |dS| must stay < 65504 */
 } fa_dtype;
 
 /*
@@ -67,7 +69,7 @@ typedef enum {
  *   scale      : multiplies q.k before the softmax (1/sqrt(d) for standard attention); finite
  *                and > 0
  *   causal     : nonzero = mask keys j > i
- *   block_mask : nullable; [T,T] uint8 tile mask (0 = tile skipped)
+ *   block_mask : nullable; [T,T] uint8 tile mask (0 = tile skipped); with a mask, N <= 786432
  *   kv_lens    : nullable; [B] int32 valid key count per sequence (keys j >= kv_lens[b]
  *                are masked for every query; values are clamped to [0, N])
  *   stream     : cudaStream_t to launch on

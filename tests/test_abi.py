@@ -69,6 +69,8 @@ def test_forward_argument_checks(lib):
     assert fwd(lib, d=96) == UNSUPPORTED
     assert fwd(lib, d=32) == UNSUPPORTED
     assert fwd(lib, dtype=7) == UNSUPPORTED
+    assert fwd(lib, dtype=3) == UNSUPPORTED
+    assert fwd(lib, dtype=2, N=0) == OK          # FA_FP16 is a supported dtype
     assert fwd(lib, B=-1) == INVALID
     assert fwd(lib, N=-5) == INVALID
     assert fwd(lib, scale=float("nan")) == INVALID

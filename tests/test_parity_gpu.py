@@ -92,6 +92,24 @@ def test_bf16_extreme_logits(d):
     check_backward_given_o(x)
 
 
+# --- fp16 inputs (same kernels, fp16 operands) -----------------------------------------------
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N,causal", [(127, False), (300, True), (1000, False), (1000, True)])
+def test_fp16_shapes(N, d, causal):
+    x = _case(N, d, "fp16", causal, seed=N + d)
+    compare(x, run_gpu(x))
+    check_backward_given_o(x)
+
+
+def test_fp16_masks():
+    x = _case(900, 128, "fp16", True, B=3, H=2, seed=8)
+    x["kv_lens"] = torch.tensor([900, 451, 0], dtype=torch.int32)
+    x["block_mask"] = random_tile_mask(8, 0.6, seed=4)
+    compare_fwd(x, run_gpu(x, backward=False))
+    check_backward_given_o(x)
+
+
 def test_empty_problem_is_noop():
     import exact_io_aware_23_gb300 as fa
     q = torch.empty((2, 3, 0, 64), dtype=torch.bfloat16, device="cuda")

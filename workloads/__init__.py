@@ -27,7 +27,7 @@ class Workload:
     H: int
     N: int
     d: int
-    dtype: str            # "bf16" or "fp32"
+    dtype: str            # "bf16", "fp16" or "fp32"
     causal: bool = False
     value_scale: float = 1.0          # Q/K/V are N(0,1) times this
     pad_lengths: Optional[tuple] = None  # (lo, hi): per-sequence valid key length ~ U{lo..hi}
@@ -72,7 +72,7 @@ def local_global_tile_mask(n_tiles: int, band: int = 4, n_global: int = 2) -> to
 
 
 def torch_dtype(name: str) -> torch.dtype:
-    return {"bf16": torch.bfloat16, "fp32": torch.float32}[name]
+    return {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[name]
 
 
 def make_inputs(w: Workload, seed: int = 0, heads: Optional[int] = None, N: Optional[int] = None,
