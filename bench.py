@@ -326,6 +326,78 @@ def run_ours(args, w):
 LAUNCHES_PER_STEP = 4
 
 
+def run_decode(args, w):
+    """Decode-shaped workloads: one step = one split-KV forward (fa_forward_splitkv); the bound is
+    HBM (the key/value cache is read once), so the roofline is reported in GB/s."""
+    import torch
+
+    import exact_io_aware_23_gb300 as fa
+    from workloads import make_inputs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    x = make_inputs(w, seed=0)
+    B, H, Nq, d = x["q"].shape
+    Nk = x["k"].shape[2]
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    splits = int(fa.lib.fa_forward_splitkv_auto_splits(B, H, Nq, Nk))
+    ws = torch.empty(int(fa.lib.fa_forward_splitkv_workspace_size(B, H, Nq, d, splits)), dtype=torch.uint8, device=dev)
+    step = lambda: fa.forward_splitkv(q, k, v, scale=w.scale, n_splits=splits, o=o, lse=lse, workspace=ws)
+    for _ in range(args.warmup):
+        step()
+    stream = torch.cuda.current_stream()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with ClockSampler(0) as clocks:
+        s0.record(stream)
+        for _ in range(args.steps):
+            step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1) / args.steps
+    if fa.check_device_status() != 0:
+        raise RuntimeError("device error during the timed region")
+    hin = [t.pin_memory() for t in (x["q"], x["k"], x["v"])]
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
+
+    def e2e_step():
+        for dst, src in zip((q, k, v), hin):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(hout, (o, lse)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    F = 4.0 * B * H * Nq * Nk * d
+    elt = q.element_size()
+    algo_bytes = elt * (2 * B * H * Nk * d + 2 * B * H * Nq * d) + 4 * B * H * Nq
+    peaks, src = load_peaks()
+    gbs = algo_bytes / (ms * 1e-3) / 1e9
+    line = {"metric": METRIC, "value": F / (ms * 1e-3) / 1e12, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": dict(workload_config(w), Nk=Nk, n_splits=splits, forward_only=True),
+            "roofline": {"bound": "hbm", "kernel": "fa_forward_splitkv (split kernel + merge)",
+                         "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                         "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                         "peak_source": f"hbm_gbs of {src}"},
+            "e2e": {"value": F / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
+                    "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout)},
+            "gpu_launches": 2 * args.steps, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -341,6 +413,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif w.Nk is not None:
+        run_decode(args, w)
     else:
         run_ours(args, w)
 

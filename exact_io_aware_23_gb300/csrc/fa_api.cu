@@ -96,9 +96,69 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
   // Masks make the work per tile unequal: then every slice's heaviest tiles go first.  Without
   // them, the tiles of one slice run together so its K/V (or Q/dO) stream is shared in L2.
   a.heads_fastest = (a.causal || block_mask != nullptr || kv_lens != nullptr) ? 1 : 0;
+  a.Nk = N; a.n_splits = 1; a.tiles_per_split = 0; a.o_part = nullptr; a.lse_part = nullptr;
   if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = dtype == FA_FP32 ? fa::launch_fwd_simt(a, dtype, s) : fa::launch_fwd_sm103(a, dtype, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_forward_splitkv_auto_splits(int B, int H, int Nq, int Nk) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return 1;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long units = (long long)B * H * ((Nq + 255) / 256);   // CTAs without splitting
+  const int kv_tiles = (Nk + 127) / 128;
+  long long want = (2LL * sms + units - 1) / units;                 // about two CTAs per SM
+  want = want < 1 ? 1 : want;
+  const long long cap = (kv_tiles + 1) / 2 < 64 ? (kv_tiles + 1) / 2 : 64;   // >= 2 tiles each
+  if (want > cap) want = cap < 1 ? 1 : cap;
+  return (int)want;
+}
+
+size_t fa_forward_splitkv_workspace_size(int B, int H, int Nq, int d, int n_splits) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || d <= 0 || n_splits <= 0) return 0;
+  const size_t rows = (size_t)n_splits * B * H * Nq;
+  return round_up(rows * (size_t)d * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+}
+
+fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int Nq, int Nk, int d, float scale,
+                             const int32_t* kv_lens, fa_dtype dtype, int n_splits,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  fa_status st = check_common(B, H, Nq, d, scale, dtype);
+  if (st != FA_OK) return st;
+  if (Nk < 0 || n_splits < 0) return FA_ERR_INVALID_ARG;
+  if (dtype == FA_FP32) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || Nq == 0) return FA_OK;
+  if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
+  const int kv_tiles = (Nk + 127) / 128;
+  if (n_splits == 0) n_splits = fa_forward_splitkv_auto_splits(B, H, Nq, Nk);
+  if (n_splits > kv_tiles) n_splits = kv_tiles > 0 ? kv_tiles : 1;
+  if ((size_t)B * H * ((Nq + 255) / 256) * (size_t)n_splits > (size_t)0x7fffffff) return FA_ERR_UNSUPPORTED;
+  if (workspace_bytes < fa_forward_splitkv_workspace_size(B, H, Nq, d, n_splits)) return FA_ERR_INVALID_ARG;
+  fa::FwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.B = B; a.H = H; a.N = Nq; a.d = d; a.scale = scale; a.causal = 0;
+  a.block_mask = nullptr; a.n_tiles = (Nq + fa::kMaskTile - 1) / fa::kMaskTile;
+  a.kv_lens = kv_lens; a.dbg = knobs(); a.heads_fastest = kv_lens != nullptr ? 1 : 0;
+  a.Nk = Nk; a.n_splits = n_splits; a.tiles_per_split = (kv_tiles + n_splits - 1) / n_splits;
+  const size_t rows = (size_t)B * H * Nq;
+  a.o_part = static_cast<float*>(workspace);
+  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        round_up((size_t)n_splits * rows * d * sizeof(float), 256));
+  if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_fwd_sm103(a, dtype, s);
+  if (e == cudaSuccess) {
+    fa::SplitMergeArgs m{};
+    m.o_part = a.o_part; m.lse_part = a.lse_part; m.o = o; m.lse = lse;
+    m.rows = (int)rows; m.d = d; m.n_splits = n_splits;
+    e = fa::launch_splitkv_merge(m, dtype, s);
+  }
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

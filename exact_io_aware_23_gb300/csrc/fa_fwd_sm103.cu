@@ -70,6 +70,8 @@ static_assert(sizeof(Bars) <= 256, "the live-tile bitmap starts 256 bytes after 
 // Per-CTA tile geometry: which key tiles exist and how each Q tile must treat them.
 struct Geo {
   int bh;          // (b, h) slice
+  int split;       // key-tile range (split-KV)
+  int j0;          // first key tile of this CTA's range
   int q0;          // first query row of Q tile 0
   int N, kv_lim;   // keys with j >= kv_lim are masked (padding and tail)
   int causal;
@@ -121,18 +123,22 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // Work order.  With masks, the (b, h) slice varies fastest, so every slice's heaviest Q-tile
     // pair runs in the first waves (the last pairs when causal, the global rows of a
     // block-sparse mask).  Without, one slice's pairs run together and share its K/V stream in L2.
+    // Split-KV: the range of key tiles varies slowest.
     const int BH = a.B * a.H;
     const int n_pairs = (a.N + 2 * BM - 1) / (2 * BM);
-    const int bh = a.heads_fastest ? (int)(blockIdx.x % BH) : (int)(blockIdx.x / n_pairs);
-    const int slot = a.heads_fastest ? (int)(blockIdx.x / BH) : (int)(blockIdx.x % n_pairs);
+    const int unit = blockIdx.x % (n_pairs * BH);
+    const int split = blockIdx.x / (n_pairs * BH);
+    const int bh = a.heads_fastest ? unit % BH : unit / n_pairs;
+    const int slot = a.heads_fastest ? unit / BH : unit % n_pairs;
     const int pair = a.causal ? n_pairs - 1 - slot : slot;
     const int b = bh / a.H;
     Geo g;
     g.bh = bh;
+    g.split = split;
     g.q0 = pair * 2 * BM;
     g.N = a.N;
-    int kvl = a.N;
-    if (a.kv_lens != nullptr) kvl = max(0, min(a.N, (int)a.kv_lens[b]));
+    int kvl = a.Nk;
+    if (a.kv_lens != nullptr) kvl = max(0, min(a.Nk, (int)a.kv_lens[b]));
     g.kv_lim = kvl;
     g.causal = a.causal;
     g.bm = a.block_mask;
@@ -140,6 +146,11 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     int last_key = g.kv_lim;
     if (a.causal) last_key = min(last_key, min(g.q0 + 2 * BM, a.N));
     g.j_end = (last_key + BN - 1) / BN;
+    g.j0 = 0;
+    if (a.n_splits > 1) {
+      g.j0 = min(split * a.tiles_per_split, g.j_end);
+      g.j_end = min(g.j_end, g.j0 + a.tiles_per_split);
+    }
     g.bits = a.block_mask != nullptr ? live_bits : nullptr;
     return g;
   };
@@ -194,7 +205,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           ptx::tma_load_3d(sQ + t * C::kTileBytes + hh * BM * 128, &tmQ, qbar, hh * 64, g.q0 + t * BM, bh);
       int n = 0;
       bool ok = true;
-      for (int j = g.next(0); j < g.j_end && ok; j = g.next(j + 1)) {
+      for (int j = g.next(g.j0); j < g.j_end && ok; j = g.next(j + 1)) {
         for (int kind = 0; kind < 2 && ok; ++kind, ++n) {
           const int slot = n % C::kSlots;
           const uint32_t ph = (n / C::kSlots) & 1;
@@ -221,7 +232,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       int n = 0, idx = 0;
       int prev_v = -1;
       uint32_t prev_vph = 0;
-      for (int j = g.next(0); j < g.j_end && ok; j = g.next(j + 1), ++idx) {
+      for (int j = g.next(g.j0); j < g.j_end && ok; j = g.next(j + 1), ++idx) {
         const int kslot = n % C::kSlots;
         const uint32_t kph = (n / C::kSlots) & 1;
         ++n;
@@ -298,12 +309,12 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const uint32_t tS = tmem + lane_off + t * BN;
     const uint32_t tO = tmem + lane_off + 256 + t * D;
     const float c = a.scale * kLog2e;               // scores -> log2 domain
-    int row_lim = min(g.kv_lim, a.N);
+    int row_lim = g.kv_lim;
     if (a.causal) row_lim = min(row_lim, i + 1);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     int idx = 0;
-    for (int j = g.next(0); j < g.j_end; j = g.next(j + 1), ++idx) {
+    for (int j = g.next(g.j0); j < g.j_end; j = g.next(j + 1), ++idx) {
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[t]), idx & 1, lim_ms, a.err);
       if (!ok) break;
       ptx::tc_fence_after();
@@ -394,6 +405,9 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const bool any = l_run > 0.f;
     const float inv = any ? 1.f / l_run : 0.f;
     uint16_t* orow = static_cast<uint16_t*>(a.o) + ((size_t)bh * a.N + i) * D;
+    // split-KV: this range's normalised partial output (fp32) and log-sum-exp
+    const size_t prow = ((size_t)g.split * a.B * a.H + bh) * a.N + i;
+    float* porow = a.o_part != nullptr ? a.o_part + prow * D : nullptr;
 #pragma unroll 1
     for (int q4 = 0; q4 < D / 32; ++q4) {
       uint32_t o[32];
@@ -405,7 +419,13 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = 0u;
       }
-      if (i < a.N) {
+      if (i < a.N && porow != nullptr) {
+        float4* dst = reinterpret_cast<float4*>(porow + q4 * 32);
+#pragma unroll
+        for (int v4 = 0; v4 < 8; ++v4)
+          dst[v4] = make_float4(__uint_as_float(o[4 * v4 + 0]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
+                                __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
+      } else if (i < a.N) {
         uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4) {
@@ -418,7 +438,11 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
     }
-    if (i < a.N) a.lse[(size_t)bh * a.N + i] = any ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+    if (i < a.N) {
+      const float L = any ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      if (porow != nullptr) a.lse_part[prow] = L;
+      else a.lse[(size_t)bh * a.N + i] = L;
+    }
   }
 
   ptx::tc_fence_before();
@@ -444,8 +468,8 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   const int BH = a.B * a.H;
   cudaError_t e;
   if ((e = make_map(&mq, a.q, D, a.N, BH, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, a.k, D, a.N, BH, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, a.v, D, a.N, BH, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, a.k, D, a.Nk, BH, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.v, D, a.Nk, BH, F16)) != cudaSuccess) return e;
   auto kern = fwd_sm103_kernel<D, F16>;
   // + the live-tile bitmap of a block-sparse mask (one bit per key tile)
   const int smem = Cfg<D, F16>::kSmem + (a.block_mask != nullptr ? ((a.n_tiles + 127) / 128) * 16 : 0);
@@ -456,7 +480,7 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   cudaFuncAttributes fattr;
   if ((e = cudaFuncGetAttributes(&fattr, kern)) != cudaSuccess) return e;
   if (fattr.numRegs * kThreads < 128 * 88 + 256 * 200) return cudaErrorInvalidConfiguration;
-  dim3 grid(((a.N + 2 * BM - 1) / (2 * BM)) * BH);
+  dim3 grid(((a.N + 2 * BM - 1) / (2 * BM)) * BH * a.n_splits);
   kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }

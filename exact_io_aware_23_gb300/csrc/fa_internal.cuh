@@ -34,6 +34,24 @@ struct FwdArgs {
   int* err;                   // device error word
   DebugKnobs dbg;
   int heads_fastest;          // launch order: (b, h) slice fastest (unequal work per tile)
+  // Split-KV (fa_forward_splitkv): keys per slice, key-tile ranges per Q-tile pair and the fp32
+  // partial results ([n_splits][B*H][N][d] and [n_splits][B*H][N]); Nk = N, n_splits = 1 and
+  // o_part = null for fa_forward.
+  int Nk;
+  int n_splits;
+  int tiles_per_split;
+  float* o_part;
+  float* lse_part;
+};
+
+struct SplitMergeArgs {       // combines the split-KV partials with the (m, l, u) merge law
+  const float* o_part;
+  const float* lse_part;
+  void* o;
+  float* lse;
+  int rows;                   // B * H * N
+  int d;
+  int n_splits;
 };
 
 struct BwdArgs {
@@ -67,5 +85,8 @@ cudaError_t launch_bwd_simt(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
 // scale + convert.
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
+
+// Split-KV merge: O = sum_s w_s O_s / sum_s w_s, LSE = m + ln sum_s w_s, w_s = exp(LSE_s - m).
+cudaError_t launch_splitkv_merge(const SplitMergeArgs& m, fa_dtype dt, cudaStream_t s);
 
 }  // namespace fa

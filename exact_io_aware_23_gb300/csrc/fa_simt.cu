@@ -327,6 +327,49 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_convert_kernel(BwdArgs a, siz
     dq[e] = from_f<T>(a.dq_acc[e] * a.scale);
 }
 
+// Split-KV merge ("FlashAttention：让精确注意力服从内存层次", section "Online softmax": two
+// tiles' statistics (m, l, u) merge as m = max(m_a, m_b), l = e^{m_a-m} l_a + e^{m_b-m} l_b,
+// u = e^{m_a-m} u_a + e^{m_b-m} u_b).  Each range s holds O_s = u_s / l_s and LSE_s = m_s + ln l_s,
+// so with w_s = exp(LSE_s - max LSE): O = sum w_s O_s / sum w_s, LSE = max LSE + ln sum w_s.
+// One warp per query row; a range with no allowed key (LSE_s = -inf) contributes nothing.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) splitkv_merge_kernel(SplitMergeArgs m) {
+  const int row = blockIdx.x * (kThreads / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= m.rows) return;
+  float mx = -INFINITY;
+  for (int sp = lane; sp < m.n_splits; sp += 32) mx = fmaxf(mx, m.lse_part[(size_t)sp * m.rows + row]);
+  mx = warp_max(mx);
+  constexpr int CPL = D / 32;
+  float acc[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+  float wsum = 0.f;
+  if (mx != -INFINITY) {
+    for (int sp = 0; sp < m.n_splits; ++sp) {
+      const float L = m.lse_part[(size_t)sp * m.rows + row];
+      if (L == -INFINITY) continue;
+      const float w = expf(L - mx);
+      wsum += w;
+      const float* src = m.o_part + ((size_t)sp * m.rows + row) * D;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acc[c] = fmaf(w, src[lane + 32 * c], acc[c]);
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  T* o = static_cast<T*>(m.o) + (size_t)row * D;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) o[lane + 32 * c] = from_f<T>(acc[c] * inv);
+  if (lane == 0) m.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+}
+
+template <typename T, int D>
+cudaError_t merge_launch(const SplitMergeArgs& m, cudaStream_t s) {
+  const int blocks = (m.rows + kThreads / 32 - 1) / (kThreads / 32);
+  splitkv_merge_kernel<T, D><<<blocks, kThreads, 0, s>>>(m);
+  return cudaGetLastError();
+}
+
 template <typename T, int D>
 cudaError_t fwd_launch(const FwdArgs& a, cudaStream_t s) {
   const size_t smem = sizeof(float) * (kBc * (D + 1) + kBc * D + kBr * D);
@@ -382,6 +425,11 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, fa_dtype dt, cudaStream_t s)
   if (dt == FA_FP32) return a.d == 64 ? pre_launch<float, 64>(a, s) : pre_launch<float, 128>(a, s);
   if (dt == FA_FP16) return a.d == 64 ? pre_launch<__half, 64>(a, s) : pre_launch<__half, 128>(a, s);
   return a.d == 64 ? pre_launch<__nv_bfloat16, 64>(a, s) : pre_launch<__nv_bfloat16, 128>(a, s);
+}
+
+cudaError_t launch_splitkv_merge(const SplitMergeArgs& m, fa_dtype dt, cudaStream_t s) {
+  if (dt == FA_FP16) return m.d == 64 ? merge_launch<__half, 64>(m, s) : merge_launch<__half, 128>(m, s);
+  return m.d == 64 ? merge_launch<__nv_bfloat16, 64>(m, s) : merge_launch<__nv_bfloat16, 128>(m, s);
 }
 
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a, fa_dtype dt, cudaStream_t s) {

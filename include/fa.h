@@ -79,6 +79,34 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
                      const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
                      void* stream);
 
+/*
+ * Split-KV forward for decode-shaped problems (few queries against a long key sequence) and for
+ * problems with too few (b, h) slices to fill the GPU: the key tiles of every query tile are cut
+ * into n_splits ranges processed by separate CTAs, each producing its own (O_s, LSE_s); a merge
+ * kernel then combines them with the merge law of the online-softmax statistics (m, l, u)
+ * ("FlashAttention：让精确注意力服从内存层次", section "Online softmax": statistics of two tiles
+ * combine as m = max(m_a, m_b), l = e^{m_a-m} l_a + e^{m_b-m} l_b, u = e^{m_a-m} u_a + e^{m_b-m} u_b).
+ * The result is the same function as fa_forward for Nq = Nk.
+ *   q          : [B, H, Nq, d]; k, v: [B, H, Nk, d]; o: [B, H, Nq, d]; lse: [B, H, Nq] fp32
+ *   kv_lens    : nullable; [B] valid keys per sequence (clamped to [0, Nk]); no causal or tile mask
+ *   dtype      : FA_BF16 or FA_FP16 (FA_FP32: FA_ERR_UNSUPPORTED)
+ *   n_splits   : key-tile ranges per query tile, >= 0 (0 = fa_forward_splitkv_auto_splits);
+ *                values above ceil(Nk / 128) are reduced to it
+ *   workspace  : >= fa_forward_splitkv_workspace_size(B, H, Nq, d, n_splits) bytes (with the
+ *                n_splits actually used), 256-byte aligned, caller-owned, overwritten
+ */
+fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int Nq, int Nk, int d, float scale,
+                             const int32_t* kv_lens, fa_dtype dtype, int n_splits,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of fa_forward_splitkv (fp32 partial O and LSE of every range). */
+size_t fa_forward_splitkv_workspace_size(int B, int H, int Nq, int d, int n_splits);
+
+/* The number of ranges fa_forward_splitkv uses for n_splits = 0: about two CTAs per SM of the
+ * current device, at least two key tiles per range, at most 64 ranges. */
+int fa_forward_splitkv_auto_splits(int B, int H, int Nq, int Nk);
+
 /* Bytes of workspace fa_backward needs for these sizes (a multiple of 256). */
 size_t fa_backward_workspace_size(int B, int H, int N, int d);
 

@@ -102,3 +102,23 @@ def test_backward_argument_checks(lib):
     assert bwd(workspace=ctypes.c_void_p(0x10010)) == INVALID     # not 256-byte aligned
     assert bwd(wsb=ws - 4) == INVALID
     assert bwd(N=0) == OK
+
+
+def test_splitkv_argument_checks(lib):
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_forward_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, i, vp, sz, vp]
+    lib.fa_forward_splitkv_workspace_size.argtypes = [i, i, i, i, i]
+    lib.fa_forward_splitkv_workspace_size.restype = sz
+    ws = lib.fa_forward_splitkv_workspace_size(2, 3, 16, 128, 4)
+    assert ws % 256 == 0 and ws >= 4 * 2 * 3 * 16 * 129 * 4
+    assert lib.fa_forward_splitkv_workspace_size(2, 3, 16, 128, 0) == 0
+
+    def call(dtype=0, d=128, Nk=4096, splits=4, w=P, wsb=ws, Nq=16):
+        return lib.fa_forward_splitkv(P, P, P, P, P, 2, 3, Nq, Nk, d, 0.1, None, dtype, splits, w, wsb, None)
+    assert call(dtype=1) == UNSUPPORTED          # fp32 has no split-KV path
+    assert call(d=96) == UNSUPPORTED
+    assert call(Nk=-1) == INVALID
+    assert call(splits=-2) == INVALID
+    assert call(w=None) == INVALID
+    assert call(wsb=ws - 256) == INVALID
+    assert call(Nq=0) == OK

@@ -33,6 +33,7 @@ class Workload:
     pad_lengths: Optional[tuple] = None  # (lo, hi): per-sequence valid key length ~ U{lo..hi}
     block_sparse: bool = False        # local band of 4 tiles + 2 global tiles (rows and cols)
     backward: bool = True
+    Nk: Optional[int] = None          # key length when it differs from N (decode shapes)
 
     @property
     def scale(self) -> float:
@@ -54,6 +55,9 @@ WORKLOADS = {
                                       causal=True),
     # a smaller long-context case for profiler captures (inputs still larger than L2)
     "long_n8k_d128": Workload("long_n8k_d128", 1, 16, 8192, 128, "bf16"),
+    # decode-shaped: 16 new queries per sequence against a 32K-key cache (forward only)
+    "decode_q16_k32k_d128": Workload("decode_q16_k32k_d128", 8, 16, 16, 128, "bf16",
+                                     backward=False, Nk=32768),
     # block-sparse attention B1 H8 N65536 d64, local band + global tiles
     "block_sparse_n64k_d64": Workload("block_sparse_n64k_d64", 1, 8, 65536, 64, "bf16",
                                       block_sparse=True),
@@ -86,18 +90,20 @@ def make_inputs(w: Workload, seed: int = 0, heads: Optional[int] = None, N: Opti
     B = w.B if B is None else B
     H = w.H if heads is None else heads
     N = w.N if N is None else N
+    Nk = N if w.Nk is None else w.Nk
     g = torch.Generator().manual_seed(seed)
     dt = torch_dtype(w.dtype)
     shape = (B, H, N, w.d)
+    kshape = (B, H, Nk, w.d)
     q = (torch.randn(shape, generator=g) * w.value_scale).to(dt)
-    k = (torch.randn(shape, generator=g) * w.value_scale).to(dt)
-    v = (torch.randn(shape, generator=g) * w.value_scale).to(dt)
+    k = (torch.randn(kshape, generator=g) * w.value_scale).to(dt)
+    v = (torch.randn(kshape, generator=g) * w.value_scale).to(dt)
     do = torch.randn(shape, generator=g).to(dt)
     kv_lens = None
     if w.pad_lengths is not None:
         lo, hi = w.pad_lengths
-        lo = min(lo, N)
-        hi = min(hi, N)
+        lo = min(lo, Nk)
+        hi = min(hi, Nk)
         kv_lens = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
     block_mask = None
     if w.block_sparse:
