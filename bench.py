@@ -175,7 +175,8 @@ def max_over_ranks(values, device, world):
 
 
 def workload_config(w):
-    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+    return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv or w.H, "N": w.N, "d": w.d,
+            "causal": w.causal,
             "key_padding": w.pad_lengths is not None, "block_sparse": w.block_sparse,
             "dtype": w.dtype, "parallelism": "replicas",
             "l2": "inputs larger than L2 (no flush)"}

@@ -52,6 +52,11 @@ def _load() -> ctypes.CDLL:
     L.fa_debug_set_wait_limit_ms.restype = None
     L.fa_version.argtypes = []
     L.fa_version.restype = i
+    L.fa_forward_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, vp]
+    L.fa_forward_gqa.restype = i
+    L.fa_backward_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i,
+                                  vp, vp, sz, vp]
+    L.fa_backward_gqa.restype = i
     L.fa_forward_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, i, vp, sz, vp]
     L.fa_forward_splitkv.restype = i
     L.fa_forward_splitkv_workspace_size.argtypes = [i, i, i, i, i]
@@ -79,16 +84,22 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 def _check_qkv(q, k, v):
+    """q: [B, H, N, d]; k, v: [B, Hkv, N, d] with Hkv dividing H (grouped-query attention when
+    Hkv < H).  Returns (B, H, N, d, Hkv)."""
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
         if t.dim() != 4:
             raise ValueError(f"{name} must be [B, H, N, d]")
-    if not (q.shape == k.shape == v.shape) or not (q.dtype == k.dtype == v.dtype):
-        raise ValueError("q, k, v must share shape and dtype")
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2:] != q.shape[2:] or H % Hkv != 0:
+        raise ValueError("k, v must be [B, Hkv, N, d] with Hkv dividing the query heads")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share a dtype")
     if q.dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {q.dtype}")
-    return q.shape
+    return B, H, N, d, Hkv
 
 
 def _masks(block_mask, kv_lens, B, N, device):
@@ -108,15 +119,21 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool =
             scale: Optional[float] = None, block_mask: Optional[torch.Tensor] = None,
             kv_lens: Optional[torch.Tensor] = None, o: Optional[torch.Tensor] = None,
             lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """O, LSE = attention forward (fa_forward).  q, k, v: [B, H, N, d] bf16, fp16 or fp32 on CUDA."""
-    B, H, N, d = _check_qkv(q, k, v)
+    """O, LSE = attention forward (fa_forward; fa_forward_gqa when k, v have fewer heads).
+    q: [B, H, N, d]; k, v: [B, Hkv, N, d]; bf16, fp16 or fp32 on CUDA."""
+    B, H, N, d, Hkv = _check_qkv(q, k, v)
     scale = 1.0 / d ** 0.5 if scale is None else float(scale)
     block_mask, kv_lens = _masks(block_mask, kv_lens, B, N, q.device)
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    st = lib.fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
-                        int(bool(causal)), _ptr(block_mask), _DTYPES[q.dtype], _ptr(kv_lens),
-                        _stream(stream))
+    if Hkv == H:
+        st = lib.fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
+                            int(bool(causal)), _ptr(block_mask), _DTYPES[q.dtype], _ptr(kv_lens),
+                            _stream(stream))
+    else:
+        st = lib.fa_forward_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
+                                scale, int(bool(causal)), _ptr(block_mask), _DTYPES[q.dtype],
+                                _ptr(kv_lens), _stream(stream))
     if st != FA_OK:
         raise FaError(st, "fa_forward")
     return o, lse
@@ -162,8 +179,9 @@ def backward_workspace_size(B: int, H: int, N: int, d: int) -> int:
 def backward(q, k, v, o, lse, do, *, causal: bool = False, scale: Optional[float] = None,
              block_mask=None, kv_lens=None, dq=None, dk=None, dv=None, workspace=None,
              stream=None):
-    """dQ, dK, dV = recompute-based attention backward (fa_backward)."""
-    B, H, N, d = _check_qkv(q, k, v)
+    """dQ, dK, dV = recompute-based attention backward (fa_backward; fa_backward_gqa when k, v
+    have fewer heads than q)."""
+    B, H, N, d, Hkv = _check_qkv(q, k, v)
     for name, t in (("o", o), ("do", do)):
         if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
             raise ValueError(f"{name} must match q")
@@ -177,10 +195,13 @@ def backward(q, k, v, o, lse, do, *, causal: bool = False, scale: Optional[float
     need = backward_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    st = lib.fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
-                         _ptr(dk), _ptr(dv), B, H, N, d, scale, int(bool(causal)),
-                         _ptr(block_mask), _DTYPES[q.dtype], _ptr(kv_lens), _ptr(workspace),
-                         workspace.numel() * workspace.element_size(), _stream(stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv))
+    tail = (d, scale, int(bool(causal)), _ptr(block_mask), _DTYPES[q.dtype], _ptr(kv_lens),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if Hkv == H:
+        st = lib.fa_backward(*args, B, H, N, *tail)
+    else:
+        st = lib.fa_backward_gqa(*args, B, H, Hkv, N, *tail)
     if st != FA_OK:
         raise FaError(st, "fa_backward")
     return dq, dk, dv
@@ -204,7 +225,9 @@ def backward_noalloc(q, k, v, o, lse, do, *, causal: bool = False, scale: Option
     """fa_backward_noalloc: the backward with the library's built-in scratch instead of a
     workspace (for callers that cannot allocate device memory).  Output tensors may be passed
     in so that the call itself allocates nothing."""
-    B, H, N, d = _check_qkv(q, k, v)
+    B, H, N, d, Hkv = _check_qkv(q, k, v)
+    if Hkv != H:
+        raise ValueError("fa_backward_noalloc takes one key/value head per query head")
     scale = 1.0 / d ** 0.5 if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk

@@ -44,6 +44,16 @@ fa_status check_common(int B, int H, int N, int d, float scale, fa_dtype dtype) 
   return FA_OK;
 }
 
+// Grouped heads: Hkv key/value heads shared by H query heads.  Hkv must divide H (Hkv = H is
+// plain multi-head attention); the fp32 SIMT path takes one key/value head per query head.
+fa_status check_heads(int H, int Hkv, fa_dtype dtype) {
+  if (Hkv < 0 || (H > 0 && Hkv == 0)) return FA_ERR_INVALID_ARG;
+  if (H == 0) return FA_OK;
+  if (Hkv > H || H % Hkv != 0) return FA_ERR_UNSUPPORTED;
+  if (Hkv != H && dtype == FA_FP32) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
 // A block-sparse mask is kept as a one-bit-per-tile list in shared memory: N <= 786432.
 constexpr int kMaxBlockSparseN = 786432;
 
@@ -77,11 +87,17 @@ void fa_debug_set_fault_injection(int mode) { g_inject.store(mode); }
 
 void fa_debug_set_wait_limit_ms(uint32_t ms) { g_wait_limit_ms.store(ms == 0 ? 2000u : ms); }
 
-fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
-                     int B, int H, int N, int d, float scale, int causal,
-                     const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
-                     void* stream) {
+}  // extern "C"
+
+namespace {
+
+fa_status forward_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int H, int Hkv, int N, int d, float scale, int causal,
+                       const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                       void* stream) {
   fa_status st = check_common(B, H, N, d, scale, dtype);
+  if (st != FA_OK) return st;
+  st = check_heads(H, Hkv, dtype);
   if (st != FA_OK) return st;
   if (B == 0 || H == 0 || N == 0) return FA_OK;
   if (block_mask != nullptr && N > kMaxBlockSparseN) return FA_ERR_UNSUPPORTED;
@@ -90,7 +106,7 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
     return FA_ERR_INVALID_ARG;
   fa::FwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
-  a.B = B; a.H = H; a.N = N; a.d = d; a.scale = scale; a.causal = causal != 0;
+  a.B = B; a.H = H; a.Hkv = Hkv; a.N = N; a.d = d; a.scale = scale; a.causal = causal != 0;
   a.block_mask = block_mask; a.n_tiles = (N + fa::kMaskTile - 1) / fa::kMaskTile;
   a.kv_lens = kv_lens; a.dbg = knobs();
   // Masks make the work per tile unequal: then every slice's heaviest tiles go first.  Without
@@ -101,6 +117,26 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = dtype == FA_FP32 ? fa::launch_fwd_simt(a, dtype, s) : fa::launch_fwd_sm103(a, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int N, int d, float scale, int causal,
+                     const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                     void* stream) {
+  return forward_impl(q, k, v, o, lse, B, H, H, N, d, scale, causal, block_mask, dtype, kv_lens,
+                      stream);
+}
+
+fa_status fa_forward_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int Hkv, int N, int d, float scale, int causal,
+                         const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                         void* stream) {
+  return forward_impl(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, block_mask, dtype, kv_lens,
+                      stream);
 }
 
 int fa_forward_splitkv_auto_splits(int B, int H, int Nq, int Nk) {
@@ -142,7 +178,7 @@ fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* 
   if (workspace_bytes < fa_forward_splitkv_workspace_size(B, H, Nq, d, n_splits)) return FA_ERR_INVALID_ARG;
   fa::FwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
-  a.B = B; a.H = H; a.N = Nq; a.d = d; a.scale = scale; a.causal = 0;
+  a.B = B; a.H = H; a.Hkv = H; a.N = Nq; a.d = d; a.scale = scale; a.causal = 0;
   a.block_mask = nullptr; a.n_tiles = (Nq + fa::kMaskTile - 1) / fa::kMaskTile;
   a.kv_lens = kv_lens; a.dbg = knobs(); a.heads_fastest = kv_lens != nullptr ? 1 : 0;
   a.Nk = Nk; a.n_splits = n_splits; a.tiles_per_split = (kv_tiles + n_splits - 1) / n_splits;
@@ -168,12 +204,18 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d) {
   return round_up(rows * (size_t)d * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
 }
 
-fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
-                      const void* dO, const float* lse, void* dq, void* dk, void* dv,
-                      int B, int H, int N, int d, float scale, int causal,
-                      const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
-                      void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+fa_status backward_impl(const void* q, const void* k, const void* v, const void* o,
+                        const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                        int B, int H, int Hkv, int N, int d, float scale, int causal,
+                        const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                        void* workspace, size_t workspace_bytes, void* stream) {
   fa_status st = check_common(B, H, N, d, scale, dtype);
+  if (st != FA_OK) return st;
+  st = check_heads(H, Hkv, dtype);
   if (st != FA_OK) return st;
   if (B == 0 || H == 0 || N == 0) return FA_OK;
   if (block_mask != nullptr && N > kMaxBlockSparseN) return FA_ERR_UNSUPPORTED;
@@ -190,7 +232,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   a.dq_acc = static_cast<float*>(workspace);
   a.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                      round_up(rows * (size_t)d * sizeof(float), 256));
-  a.B = B; a.H = H; a.N = N; a.d = d; a.scale = scale; a.causal = causal != 0;
+  a.B = B; a.H = H; a.Hkv = Hkv; a.N = N; a.d = d; a.scale = scale; a.causal = causal != 0;
   a.block_mask = block_mask; a.n_tiles = (N + fa::kMaskTile - 1) / fa::kMaskTile;
   a.kv_lens = kv_lens; a.dbg = knobs();
   // Masks make the work per tile unequal: then every slice's heaviest tiles go first.  Without
@@ -203,6 +245,28 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
     e = dtype == FA_FP32 ? fa::launch_bwd_simt(a, dtype, s) : fa::launch_bwd_sm103(a, dtype, s);
   if (e == cudaSuccess) e = fa::launch_bwd_dq_convert(a, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
+                      const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                      int B, int H, int N, int d, float scale, int causal,
+                      const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, N, d, scale, causal, block_mask,
+                       dtype, kv_lens, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const void* o,
+                          const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                          int B, int H, int Hkv, int N, int d, float scale, int causal,
+                          const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal, block_mask,
+                       dtype, kv_lens, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_check_device_status(void* stream) {

@@ -7,8 +7,9 @@
 //     P = exp(scale*S - LSE),  dV += P^T dO,  dP = dO V^T,  dS = P * (dP - D),
 //     dK += scale * dS^T Q,  dQ += scale * dS K.
 //
-// GB300 design: one CTA per 128-key tile j of one (b, h) slice, 320 threads, looping over every
-// live 128-row query tile i.  The transposed products keep the key rows on the TMEM lanes, so
+// GB300 design: one CTA per 128-key tile j of one (b, h) key/value slice, 320 threads, looping
+// over every live 128-row query tile i of every query head that reads that slice (one head,
+// or the G heads of a group under grouped-query attention).  The transposed products keep the key rows on the TMEM lanes, so
 // one thread owns one key row of S^T, dP^T, P^T and dS^T:
 //   warp 8      TMA producer: K_j, V_j once; Q_i, dO_i through a two-stage ring, with the
 //               tile's LSE (as a log2-domain bias) and D vectors staged beside them.
@@ -126,11 +127,16 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   // Work order.  With masks, the (b, h) slice varies fastest, so every slice's heaviest key
   // tiles (the first ones when causal, the global columns of a block-sparse mask) run in the
   // first waves.  Without, one slice's key tiles run together and share its Q/dO stream in L2.
-  const int BH = a.B * a.H;
+  // A CTA owns one key tile of one key/value head; with grouped-query attention the G = H / Hkv
+  // query heads that share that key/value head are all visited by it, so dK and dV accumulate
+  // over the whole group on chip.
+  const int BH = a.B * a.Hkv;
   const int n_kt = (a.N + BN - 1) / BN;
-  const int bh = a.heads_fastest ? (int)(blockIdx.x % BH) : (int)(blockIdx.x / n_kt);
+  const int bh = a.heads_fastest ? (int)(blockIdx.x % BH) : (int)(blockIdx.x / n_kt);   // K/V slice
   const int jt = a.heads_fastest ? (int)(blockIdx.x / BH) : (int)(blockIdx.x % n_kt);   // key tile
-  const int b = bh / a.H;
+  const int b = bh / a.Hkv;
+  const int G = a.H / a.Hkv;
+  const int bhq0 = b * a.H + (bh % a.Hkv) * G;   // first query slice of the group
   const uint32_t lim_ms = a.dbg.wait_limit_ms;
 
   Geo g;
@@ -194,7 +200,9 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           ptx::tma_load_3d(sbase + C::kV + hh * 128 * 128, &tmV, kb, hh * 64, g.k0, bh);
         }
       }
+      for (int hg = 0; hg < G && ok; ++hg)
       for (int i = g.next(g.i_begin); i < g.i_end && ok; i = g.next(i + 1), ++n) {
+        const int bhq = bhq0 + hg;
         const int st = n & 1;
         const uint32_t ph = (n >> 1) & 1;
         if (lane == 0) ok = ptx::mbar_wait(ptx::smem_u32(&bars->st_empty[st]), ph ^ 1, lim_ms, a.err);
@@ -205,9 +213,9 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         float* dl = lse2 + 128;
         for (int r = lane; r < 128; r += 32) {
           const int q = i * BM + r;
-          float L = q < a.N ? a.lse[(size_t)bh * a.N + q] : -INFINITY;
+          float L = q < a.N ? a.lse[(size_t)bhq * a.N + q] : -INFINITY;
           lse2[r] = L == -INFINITY ? -INFINITY : -L * kLog2e;   // stored negated
-          dl[r] = q < a.N ? a.delta[(size_t)bh * a.N + q] : 0.f;
+          dl[r] = q < a.N ? a.delta[(size_t)bhq * a.N + q] : 0.f;
         }
         __syncwarp();
         if (lane == 0) {
@@ -215,8 +223,8 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           ptx::mbar_arrive_expect_tx(fb, 2 * C::kTile);
           const uint32_t sq = sbase + C::kQ0 + st * 2 * C::kTile;
           for (int hh = 0; hh < D / 64; ++hh) {
-            ptx::tma_load_3d(sq + hh * 128 * 128, &tmQ, fb, hh * 64, i * BM, bh);
-            ptx::tma_load_3d(sq + C::kTile + hh * 128 * 128, &tmDO, fb, hh * 64, i * BM, bh);
+            ptx::tma_load_3d(sq + hh * 128 * 128, &tmQ, fb, hh * 64, i * BM, bhq);
+            ptx::tma_load_3d(sq + C::kTile + hh * 128 * 128, &tmDO, fb, hh * 64, i * BM, bhq);
           }
         }
       }
@@ -233,6 +241,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       int n = 0;
       if (g.next(g.i_begin) < g.i_end) {
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, lim_ms, a.err);
+        for (int hg = 0; hg < G && ok; ++hg)
         for (int i = g.next(g.i_begin); i < g.i_end && ok; i = g.next(i + 1), ++n) {
           const int st = n & 1;
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->st_full[st]), (n >> 1) & 1, lim_ms, a.err);
@@ -311,7 +320,9 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     bool ok = true;
     int n = 0;
     int pend_st = -1;                                // stage whose staged dQ is still being read
+    for (int hg = 0; hg < G && ok; ++hg)
     for (int i = g.next(g.i_begin); i < g.i_end; i = g.next(i + 1), ++n) {
+      const int bhq = bhq0 + hg;
       const int st = n & 1;
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->st_full[st]), (n >> 1) & 1, lim_ms, a.err);
       if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full), n & 1, lim_ms, a.err);
@@ -451,7 +462,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
             for (int bx = 0; bx < kBoxes; ++bx)
               ptx::tma_reduce_add_3d(&tmDQ, ptx::smem_u32(stage + ((wg * kBoxes + bx) * 4 + sub) * 4096),
-                                     wg * (D / 2) + bx * 32, row0, bh);
+                                     wg * (D / 2) + bx * 32, row0, bhq);
             ptx::bulk_commit();
           }
           pend_st = st;   // handed back to the producer once the TMA unit has read it
@@ -516,11 +527,12 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH, boo
 template <int D, bool F16>
 cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv, mdo, mdq;
-  const int BH = a.B * a.H;
+  const int BH = a.B * a.H;            // query slices (Q, dO, dQ)
+  const int BHkv = a.B * a.Hkv;        // key/value slices (K, V, dK, dV)
   cudaError_t e;
   if ((e = make_map(&mq, a.q, D, a.N, BH, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, a.k, D, a.N, BH, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, a.v, D, a.N, BH, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, a.k, D, a.N, BHkv, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.v, D, a.N, BHkv, F16)) != cudaSuccess) return e;
   if ((e = make_map(&mdo, a.dO, D, a.N, BH, F16)) != cudaSuccess) return e;
   {
     // fp32 dQ workspace viewed as (d, N, B*H); boxes of 32 columns x 32 rows
@@ -538,7 +550,7 @@ cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
   if (a.block_mask != nullptr) smem = max(smem, Cfg<D, F16>::kBar + 128 + ((a.n_tiles + 127) / 128) * 16);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(((a.N + BN - 1) / BN) * BH);
+  dim3 grid(((a.N + BN - 1) / BN) * BHkv);
   kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mdo, mdq, a);
   return cudaGetLastError();
 }

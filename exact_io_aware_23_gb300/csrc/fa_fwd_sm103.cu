@@ -193,6 +193,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     ptx::regs_dec<88>();
     const Geo g = make_geo();
     const int bh = g.bh;
+    // grouped-query attention: query head h reads key/value head h / (H / Hkv)
+    const int bh_kv = (bh / a.H) * a.Hkv + (bh % a.H) / (a.H / a.Hkv);
     if (warp == 8 && lane == 0) {
       // ------------------------------- TMA producer -------------------------------------------
       ptx::tma_prefetch_desc(&tmQ);
@@ -216,7 +218,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
           const CUtensorMap* m = kind == 0 ? &tmK : &tmV;
           for (int hh = 0; hh < D / 64; ++hh)
-            ptx::tma_load_3d(sKV + slot * C::kTileBytes + hh * BN * 128, m, fb, hh * 64, j * BN, bh);
+            ptx::tma_load_3d(sKV + slot * C::kTileBytes + hh * BN * 128, m, fb, hh * 64, j * BN, bh_kv);
         }
       }
       // Drain: every copy this CTA issued must have landed before shared memory is released.
@@ -468,8 +470,8 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   const int BH = a.B * a.H;
   cudaError_t e;
   if ((e = make_map(&mq, a.q, D, a.N, BH, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, a.k, D, a.Nk, BH, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, a.v, D, a.Nk, BH, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, a.k, D, a.Nk, a.B * a.Hkv, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.v, D, a.Nk, a.B * a.Hkv, F16)) != cudaSuccess) return e;
   auto kern = fwd_sm103_kernel<D, F16>;
   // + the live-tile bitmap of a block-sparse mask (one bit per key tile)
   const int smem = Cfg<D, F16>::kSmem + (a.block_mask != nullptr ? ((a.n_tiles + 127) / 128) * 16 : 0);

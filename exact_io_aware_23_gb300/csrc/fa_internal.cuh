@@ -26,6 +26,7 @@ struct FwdArgs {
   void* o;
   float* lse;
   int B, H, N, d;
+  int Hkv;                    // key/value heads (H for plain attention; H / G with grouped queries)
   float scale;
   int causal;
   const uint8_t* block_mask;  // [T, T] or null
@@ -67,6 +68,7 @@ struct BwdArgs {
   float* dq_acc;    // workspace: fp32 [B, H, N, d]
   float* delta;     // workspace: fp32 [B, H, N], D_i = rowsum(dO_i * O_i)
   int B, H, N, d;
+  int Hkv;          // key/value heads (K, V, dK, dV are [B, Hkv, N, d])
   float scale;
   int causal;
   const uint8_t* block_mask;

@@ -80,6 +80,25 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
                      void* stream);
 
 /*
+ * Grouped-query attention (the pages list "GQA head mapping" among the semantics production use
+ * needs: "FlashAttention：让精确注意力服从内存层次", list after the CPU reference): H query heads
+ * share Hkv key/value heads, query head h reading key/value head h / (H / Hkv).  K and V (and, in
+ * the backward, dK and dV) are [B, Hkv, N, d]; Q, O, dO, dQ are [B, H, N, d]; LSE is [B, H, N].
+ * dK and dV of a key/value head sum the contributions of all query heads of its group.
+ * Hkv must divide H; bf16 or fp16 only (FA_ERR_UNSUPPORTED otherwise).  Hkv = H is fa_forward /
+ * fa_backward.  The backward's workspace is fa_backward_workspace_size(B, H, N, d).
+ */
+fa_status fa_forward_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int Hkv, int N, int d, float scale, int causal,
+                         const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                         void* stream);
+fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const void* o,
+                          const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                          int B, int H, int Hkv, int N, int d, float scale, int causal,
+                          const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Split-KV forward for decode-shaped problems (few queries against a long key sequence) and for
  * problems with too few (b, h) slices to fill the GPU: the key tiles of every query tile are cut
  * into n_splits ranges processed by separate CTAs, each producing its own (O_s, LSE_s); a merge

@@ -32,6 +32,13 @@ What it computes, and where the pages fix it:
   (m, l, u) merge law) so that the dense oracle can be checked against the pages' claim that the
   two agree (page 3, "CPU reference": error below 1e-12 on its worked example).
 
+* Grouped-query attention (page 3, list after the CPU reference: "GQA head mapping" among the
+  production semantics).  The pages name the feature only; the oracle takes the usual reading:
+  with H query heads and Hkv key/value heads (Hkv dividing H), query head h attends with
+  key/value head h // (H / Hkv), so consecutive query heads share one key/value head.  In the
+  backward, dK and dV of a key/value head are the sums over the query heads that read it (the
+  chain rule through the shared operand).
+
 Large inputs are processed a chunk of query rows at a time (a memory bound only: each chunk
 still forms its full score rows).  When a tile mask removes most columns, a chunk gathers
 the columns that any of its rows may attend to; every other column is masked for the whole
@@ -52,6 +59,13 @@ def _as_i64_list(x, B: int) -> list:
     if x is None:
         return [None] * B
     return [int(v) for v in np.asarray(x).reshape(-1)]
+
+
+def kv_head(h: int, H: int, Hkv: int) -> int:
+    """Key/value head read by query head h when H query heads share Hkv key/value heads."""
+    if Hkv <= 0 or H % Hkv != 0:
+        raise ValueError("the key/value heads must divide the query heads")
+    return h // (H // Hkv)
 
 
 def allowed(rows: np.ndarray, cols: np.ndarray, causal: bool, kv_len: Optional[int],
@@ -104,9 +118,11 @@ def forward(q, k, v, scale: float, causal: bool = False, kv_lens=None, block_mas
             rows: Optional[Sequence[int]] = None, heads: Optional[Sequence[int]] = None):
     """Dense masked attention in fp64.
 
-    q, k, v: float64 arrays [B, H, N, d] (k and v may have a different N only when neither
-    causal nor a block mask is set).  Returns (O [B,H,R,d], LSE [B,H,R]) for the R query rows
-    in ``rows`` (default: all rows) and the heads in ``heads`` (default: all heads).
+    q: float64 array [B, H, N, d]; k, v: [B, Hkv, N, d] with Hkv dividing H (query head h reads
+    key/value head h // (H / Hkv); Hkv = H is ordinary multi-head attention).  k and v may have
+    a different N only when neither causal nor a block mask is set.  Returns
+    (O [B,H,R,d], LSE [B,H,R]) for the R query rows in ``rows`` (default: all rows) and the
+    heads in ``heads`` (default: all heads).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -116,18 +132,20 @@ def forward(q, k, v, scale: float, causal: bool = False, kv_lens=None, block_mas
     rows = np.arange(Nq) if rows is None else np.asarray(rows, dtype=np.int64)
     heads = list(range(H)) if heads is None else list(heads)
     lens = _as_i64_list(kv_lens, B)
+    Hkv = k.shape[1]
     O = np.zeros((B, len(heads), rows.size, v.shape[3]))
     L = np.full((B, len(heads), rows.size), -np.inf)
     for b in range(B):
         for hi, h in enumerate(heads):
+            g = kv_head(h, H, Hkv)
             for c0 in range(0, rows.size, ROW_CHUNK):
                 r = rows[c0:c0 + ROW_CHUNK]
                 cols = _chunk_cols(r, Nk, causal, lens[b], block_mask)
                 ok = allowed(r, cols, causal, lens[b], block_mask)
-                s = _scores(q[b, h, r], k[b, h, cols], scale, ok)
+                s = _scores(q[b, h, r], k[b, g, cols], scale, ok)
                 lse = _row_lse(s)
                 p = _probs(s, lse)
-                O[b, hi, c0:c0 + r.size] = p @ v[b, h, cols]
+                O[b, hi, c0:c0 + r.size] = p @ v[b, g, cols]
                 L[b, hi, c0:c0 + r.size] = lse
     return O, L
 
@@ -147,6 +165,9 @@ def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, bloc
     """Explicit-gradient backward of dense masked attention, fp64.
 
     Returns (dQ, dK, dV), each [B, len(heads), N, d]; with ``return_delta`` also D [B,H',N].
+    With fewer key/value heads than query heads (k, v [B, Hkv, N, d]; see ``forward``), dK and
+    dV are [B, Hkv, N, d] and each key/value head sums the contributions of the selected query
+    heads that read it.
     D_i = sum_j P_ij dP_ij, the exact gradient's row term.  When the forward output ``o``
     ([B,H,N,d]) is given, D_i = sum_c dO_ic o_ic instead: the backward as an operator of its
     inputs (q, k, v, o, dO, LSE), the form the method's backward takes (equal to the first
@@ -161,28 +182,32 @@ def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, bloc
     B, H, N, d = q.shape
     heads = list(range(H)) if heads is None else list(heads)
     lens = _as_i64_list(kv_lens, B)
+    Hkv = k.shape[1]
+    grouped = Hkv != H
     dQ = np.zeros((B, len(heads), N, d))
-    dK = np.zeros((B, len(heads), k.shape[2], d))
-    dV = np.zeros((B, len(heads), v.shape[2], v.shape[3]))
+    dK = np.zeros((B, Hkv if grouped else len(heads), k.shape[2], d))
+    dV = np.zeros((B, Hkv if grouped else len(heads), v.shape[2], v.shape[3]))
     Dd = np.zeros((B, len(heads), N))
     all_rows = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
     for b in range(B):
         for hi, h in enumerate(heads):
+            g = kv_head(h, H, Hkv)
+            kvi = g if grouped else hi
             for c0 in range(0, all_rows.size, ROW_CHUNK):
                 r = all_rows[c0:c0 + ROW_CHUNK]
                 cols = _chunk_cols(r, k.shape[2], causal, lens[b], block_mask)
                 ok = allowed(r, cols, causal, lens[b], block_mask)
-                s = _scores(q[b, h, r], k[b, h, cols], scale, ok)
+                s = _scores(q[b, h, r], k[b, g, cols], scale, ok)
                 p = _probs(s, _row_lse(s))
-                dp = do[b, h, r] @ v[b, h, cols].T
+                dp = do[b, h, r] @ v[b, g, cols].T
                 if o is None:
                     D = (p * dp).sum(axis=1)
                 else:
                     D = (do[b, h, r] * np.asarray(o, dtype=np.float64)[b, h, r]).sum(axis=1)
                 ds = p * (dp - D[:, None])
-                dQ[b, hi, r] = scale * (ds @ k[b, h, cols])
-                dK[b, hi, cols] += scale * (ds.T @ q[b, h, r])
-                dV[b, hi, cols] += p.T @ do[b, h, r]
+                dQ[b, hi, r] = scale * (ds @ k[b, g, cols])
+                dK[b, kvi, cols] += scale * (ds.T @ q[b, h, r])
+                dV[b, kvi, cols] += p.T @ do[b, h, r]
                 Dd[b, hi, r] = D
     if return_delta:
         return dQ, dK, dV, Dd

@@ -83,9 +83,11 @@ def compare_bwd(x, grads, heads=None, o_given=None):
     og = None if o_given is None else o_given
     dQ, dK, dV = oracle.backward(qq, kk, vv, dd, x["scale"], causal=x["causal"], kv_lens=kv,
                                  block_mask=bm, heads=hs, o=og)
+    grouped = kk.shape[1] != H          # dK, dV then hold the key/value heads' group sums
+    assert not (grouped and heads is not None)
     res = {}
     for name, key, ref in (("dQ", "dq", dQ), ("dK", "dk", dK), ("dV", "dv", dV)):
-        got = f64(grads[key])[:, hs]
+        got = f64(grads[key]) if grouped and key != "dq" else f64(grads[key])[:, hs]
         if x["dtype"] == "fp32":
             res[name] = assert_fp32_close(name, got, ref, FP32_MAX_ABS)
         else:

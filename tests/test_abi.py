@@ -122,3 +122,28 @@ def test_splitkv_argument_checks(lib):
     assert call(w=None) == INVALID
     assert call(wsb=ws - 256) == INVALID
     assert call(Nq=0) == OK
+
+
+def test_gqa_argument_checks(lib):
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_forward_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, vp]
+    lib.fa_backward_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i,
+                                    vp, vp, sz, vp]
+    ws = lib.fa_backward_workspace_size(2, 8, 100, 64)
+
+    def fwd_g(H=8, Hkv=2, N=128, dtype=0, q=P):
+        return lib.fa_forward_gqa(q, P, P, P, P, 2, H, Hkv, N, 64, 0.125, 1, None, dtype, None, None)
+
+    def bwd_g(H=8, Hkv=2, N=100, dtype=0, wsb=ws):
+        return lib.fa_backward_gqa(P, P, P, P, P, P, P, P, P, 2, H, Hkv, N, 64, 0.125, 1, None,
+                                   dtype, None, P, wsb, None)
+    for call in (fwd_g, bwd_g):
+        assert call(Hkv=3) == UNSUPPORTED           # 3 does not divide 8
+        assert call(Hkv=16) == UNSUPPORTED          # more key/value heads than query heads
+        assert call(Hkv=0) == INVALID
+        assert call(Hkv=-2) == INVALID
+        assert call(dtype=1) == UNSUPPORTED         # fp32 runs on the SIMT path, one head per head
+        assert call(N=0) == OK
+        assert call(dtype=2, N=0) == OK
+    assert fwd_g(q=None) == INVALID
+    assert bwd_g(wsb=ws - 4) == INVALID

@@ -319,6 +319,70 @@ def test_backward_finite_differences(case):
             assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(g[idx])), (name, idx, fd, g[idx])
 
 
+def test_gqa_backward_finite_differences():
+    """Grouped heads: the gradients of K and V, which several query heads share, match central
+    differences of L = sum(dO * O) over all query heads (fp64)."""
+    H, Hkv, N, d = 4, 2, 6, 3
+    q, do = (_rand((1, H, N, d), s, 1.2) for s in (140, 141))
+    k, v = (_rand((1, Hkv, N, d), s, 1.2) for s in (142, 143))
+    scale = 0.7
+    dQ, dK, dV = oracle.backward(q, k, v, do, scale, causal=True)
+    assert dK.shape == k.shape and dV.shape == v.shape and dQ.shape == q.shape
+    h = 1e-6
+    for name, x, g in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+        for f in range(x.size):
+            idx = tuple(int(i) for i in np.unravel_index(f, x.shape))
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args = {"q": q, "k": k, "v": v}
+            lp = _loss(**{**args, name: xp}, do=do, scale=scale, causal=True)
+            lm = _loss(**{**args, name: xm}, do=do, scale=scale, causal=True)
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(g[idx])), (name, idx, fd, g[idx])
+
+
+@pytest.mark.parametrize("Hkv", [1, 2, 3])
+def test_gqa_equals_attention_with_repeated_heads(Hkv):
+    """Grouped heads are ordinary multi-head attention on K, V with each key/value head repeated
+    for the H / Hkv consecutive query heads that read it; dK, dV are the group sums."""
+    B, H, N, d = 2, 6, 150, 8
+    G = H // Hkv
+    q, do = (_rand((B, H, N, d), s) for s in (150, 151))
+    k, v = (_rand((B, Hkv, N, d), s) for s in (152, 153))
+    kw = dict(causal=True, kv_lens=[150, 97])
+    O, L = oracle.forward(q, k, v, 0.4, **kw)
+    kr, vr = np.repeat(k, G, axis=1), np.repeat(v, G, axis=1)
+    O2, L2 = oracle.forward(q, kr, vr, 0.4, **kw)
+    assert np.array_equal(O, O2) and np.array_equal(L, L2)
+    dQ, dK, dV = oracle.backward(q, k, v, do, 0.4, **kw)
+    dQ2, dK2, dV2 = oracle.backward(q, kr, vr, do, 0.4, **kw)
+    assert np.array_equal(dQ, dQ2)
+    assert np.max(np.abs(dK - dK2.reshape(B, Hkv, G, N, d).sum(axis=2))) < 1e-12
+    assert np.max(np.abs(dV - dV2.reshape(B, Hkv, G, N, d).sum(axis=2))) < 1e-12
+
+
+def test_gqa_identical_query_heads():
+    """When the G query heads of a group carry the same Q and dO, every head's O equals the
+    one-head result and dK, dV are G times the one-head gradients."""
+    H, Hkv, N, d = 4, 1, 90, 4
+    q1, do1 = (_rand((1, 1, N, d), s) for s in (160, 161))
+    k, v = (_rand((1, 1, N, d), s) for s in (162, 163))
+    q, do = np.repeat(q1, H, axis=1), np.repeat(do1, H, axis=1)
+    O1, _ = oracle.forward(q1, k, v, 0.5)
+    O, _ = oracle.forward(q, k, v, 0.5)
+    assert np.array_equal(O, np.repeat(O1, H, axis=1))
+    _, dK1, dV1 = oracle.backward(q1, k, v, do1, 0.5)
+    _, dK, dV = oracle.backward(q, k, v, do, 0.5)
+    assert np.max(np.abs(dK - H * dK1)) < 1e-12 and np.max(np.abs(dV - H * dV1)) < 1e-12
+
+
+def test_gqa_head_mapping_rejects_non_divisors():
+    assert [oa.kv_head(h, 8, 2) for h in range(8)] == [0, 0, 0, 0, 1, 1, 1, 1]
+    with pytest.raises(ValueError):
+        oa.kv_head(0, 6, 4)
+
+
 def test_backward_delta_both_ways_and_sums():
     """D_i = sum_j P_ij dP_ij equals rowsum(dO * O); sum_j dK_j = 0; sum_j dV_j = sum_i dO_i."""
     B, H, N, d = 1, 2, 200, 8

@@ -1,7 +1,8 @@
 """Plant plausible mistakes in a copy of the oracle (on the CPU) and check that the pins in
 test_oracle.py catch every one: a dropped scale, a sign, a transposed operand, an off-by-one in
 each mask, the wrong logarithm base, a wrong reduction axis, a wrong rescale direction in the
-pages' online algorithm and a wrong factor in the pages' merge law."""
+pages' online algorithm, a wrong factor in the pages' merge law and a wrong query-to-key/value
+head mapping."""
 import os
 import shutil
 import subprocess
@@ -12,10 +13,10 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 MUTATIONS = [
-    ("dQ[b, hi, r] = scale * (ds @ k[b, h, cols])", "dQ[b, hi, r] = (ds @ k[b, h, cols])"),
+    ("dQ[b, hi, r] = scale * (ds @ k[b, g, cols])", "dQ[b, hi, r] = (ds @ k[b, g, cols])"),
     ("ds = p * (dp - D[:, None])", "ds = p * (dp + D[:, None])"),
-    ("dK[b, hi, cols] += scale * (ds.T @ q[b, h, r])", "dK[b, hi, cols] += scale * (ds @ q[b, h, r])"),
-    ("dV[b, hi, cols] += p.T @ do[b, h, r]", "dV[b, hi, cols] += p.T @ do[b, h, r] * 1.0001"),
+    ("dK[b, kvi, cols] += scale * (ds.T @ q[b, h, r])", "dK[b, kvi, cols] += scale * (ds @ q[b, h, r])"),
+    ("dV[b, kvi, cols] += p.T @ do[b, h, r]", "dV[b, kvi, cols] += p.T @ do[b, h, r] * 1.0001"),
     ("ok &= cols[None, :] <= rows[:, None]", "ok &= cols[None, :] < rows[:, None]"),
     ("ok &= (cols < kv_len)[None, :]", "ok &= (cols <= kv_len)[None, :]"),
     ("ok &= bm[(rows // TILE)[:, None], (cols // TILE)[None, :]]",
@@ -23,12 +24,14 @@ MUTATIONS = [
     ("s = scale * (q_rows @ k_cols.T)", "s = (q_rows @ k_cols.T)"),
     ("lse = m0 + np.log(np.exp(s - m0[:, None]).sum(axis=1))",
      "lse = m0 + np.log2(np.exp(s - m0[:, None]).sum(axis=1))"),
-    ("O[b, hi, c0:c0 + r.size] = p @ v[b, h, cols]", "O[b, hi, c0:c0 + r.size] = p @ v[b, h, cols[::-1]]"),
+    ("O[b, hi, c0:c0 + r.size] = p @ v[b, g, cols]", "O[b, hi, c0:c0 + r.size] = p @ v[b, g, cols[::-1]]"),
     ("shrink = np.exp(run_max - new_max)", "shrink = np.exp(new_max - run_max)"),
     ("D = (do[b, h, r] * np.asarray(o, dtype=np.float64)[b, h, r]).sum(axis=1)",
      "D = (q[b, h, r] * np.asarray(o, dtype=np.float64)[b, h, r]).sum(axis=1)"),
     ("return m, fa * la + fb * lb, fa * np.asarray(ua) + fb * np.asarray(ub)",
      "return m, fa * la + fb * lb, fa * np.asarray(ua) + fa * np.asarray(ub)"),
+    ("return h // (H // Hkv)", "return h % Hkv"),
+    ("kvi = g if grouped else hi", "kvi = hi % Hkv if grouped else hi"),
 ]
 
 

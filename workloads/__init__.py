@@ -34,6 +34,7 @@ class Workload:
     block_sparse: bool = False        # local band of 4 tiles + 2 global tiles (rows and cols)
     backward: bool = True
     Nk: Optional[int] = None          # key length when it differs from N (decode shapes)
+    Hkv: Optional[int] = None         # key/value heads when fewer than H (grouped-query attention)
 
     @property
     def scale(self) -> float:
@@ -58,6 +59,9 @@ WORKLOADS = {
     # decode-shaped: 16 new queries per sequence against a 32K-key cache (forward only)
     "decode_q16_k32k_d128": Workload("decode_q16_k32k_d128", 8, 16, 16, 128, "bf16",
                                      backward=False, Nk=32768),
+    # grouped-query attention: 32 query heads on 8 key/value heads, B2 N8192 d128, causal
+    "gqa_causal_n8k_h32_kv8_d128": Workload("gqa_causal_n8k_h32_kv8_d128", 2, 32, 8192, 128,
+                                            "bf16", causal=True, Hkv=8),
     # block-sparse attention B1 H8 N65536 d64, local band + global tiles
     "block_sparse_n64k_d64": Workload("block_sparse_n64k_d64", 1, 8, 65536, 64, "bf16",
                                       block_sparse=True),
@@ -80,12 +84,14 @@ def torch_dtype(name: str) -> torch.dtype:
 
 
 def make_inputs(w: Workload, seed: int = 0, heads: Optional[int] = None, N: Optional[int] = None,
-                B: Optional[int] = None) -> dict:
+                B: Optional[int] = None, kv_heads: Optional[int] = None) -> dict:
     """Draw one workload's inputs on the CPU.
 
     Returns a dict with q, k, v, do ([B,H,N,d] in the workload dtype), kv_lens (int32 [B] or
     None), block_mask (uint8 [T,T] or None), plus the scalar settings.  ``heads``/``N``/``B``
-    override the sizes for reduced test cases (same recipe, smaller tensors).
+    override the sizes for reduced test cases (same recipe, smaller tensors).  ``kv_heads``
+    gives k and v fewer heads than q (grouped-query attention); the default is the workload's
+    own key/value head count, or one key/value head per query head when ``heads`` overrides H.
     """
     B = w.B if B is None else B
     H = w.H if heads is None else heads
@@ -94,7 +100,9 @@ def make_inputs(w: Workload, seed: int = 0, heads: Optional[int] = None, N: Opti
     g = torch.Generator().manual_seed(seed)
     dt = torch_dtype(w.dtype)
     shape = (B, H, N, w.d)
-    kshape = (B, H, Nk, w.d)
+    if kv_heads is None:
+        kv_heads = w.Hkv if (w.Hkv is not None and heads is None) else H
+    kshape = (B, kv_heads, Nk, w.d)
     q = (torch.randn(shape, generator=g) * w.value_scale).to(dt)
     k = (torch.randn(kshape, generator=g) * w.value_scale).to(dt)
     v = (torch.randn(kshape, generator=g) * w.value_scale).to(dt)
