@@ -210,10 +210,11 @@ def run_ours(args, w):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa.backward_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
     kw = dict(causal=w.causal, scale=w.scale, block_mask=bm, kv_lens=kl)
+    bkw = dict(kw, deterministic=args.deterministic)
 
     def step():
         fa.forward(q, k, v, o=o, lse=lse, **kw)
-        fa.backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
+        fa.backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws, **bkw)
 
     for _ in range(args.warmup):
         step()
@@ -232,7 +233,7 @@ def run_ours(args, w):
             ev[i][0].record(stream)
             fa.forward(q, k, v, o=o, lse=lse, **kw)
             ev[i][1].record(stream)
-            fa.backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
+            fa.backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws, **bkw)
             ev[i][2].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
@@ -294,7 +295,8 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": workload_config(w),
+        "config": dict(workload_config(w),
+                       **({"deterministic_backward": True} if args.deterministic else {})),
         "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
         "fwd_bwd_tflops_algorithmic": world * 3.5 * F / (ms_step * 1e-3) / 1e12,
         "pct_of_bf16_peak": {"forward": fwd_tf / peak, "fwd_bwd": value / world / peak,
@@ -323,7 +325,8 @@ def run_ours(args, w):
         print(json.dumps(line), flush=True)
 
 
-# kernels of ours launched per step: forward 1, backward 3 (preprocess, main, dQ convert)
+# kernels of ours launched per step: forward 1, backward 3 (preprocess, main, dQ convert; with
+# --deterministic: preprocess, dK/dV kernel, dQ kernel)
 LAUNCHES_PER_STEP = 4
 
 
@@ -407,6 +410,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long_n16k_d128")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time the bit-reproducible backward (fa_backward_deterministic)")
     ap.add_argument("--cpu-rows", type=int, default=16384)
     ap.add_argument("--ref-rows", type=int, default=1024)
     args = ap.parse_args()

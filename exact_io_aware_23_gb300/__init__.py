@@ -57,6 +57,11 @@ def _load() -> ctypes.CDLL:
     L.fa_backward_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i,
                                   vp, vp, sz, vp]
     L.fa_backward_gqa.restype = i
+    L.fa_backward_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f,
+                                            i, vp, i, vp, vp, sz, vp]
+    L.fa_backward_deterministic.restype = i
+    L.fa_backward_deterministic_workspace_size.argtypes = [i, i, i]
+    L.fa_backward_deterministic_workspace_size.restype = sz
     L.fa_forward_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, i, vp, sz, vp]
     L.fa_forward_splitkv.restype = i
     L.fa_forward_splitkv_workspace_size.argtypes = [i, i, i, i, i]
@@ -176,11 +181,15 @@ def backward_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return int(lib.fa_backward_workspace_size(B, H, N, d))
 
 
+def backward_deterministic_workspace_size(B: int, H: int, N: int) -> int:
+    return int(lib.fa_backward_deterministic_workspace_size(B, H, N))
+
+
 def backward(q, k, v, o, lse, do, *, causal: bool = False, scale: Optional[float] = None,
              block_mask=None, kv_lens=None, dq=None, dk=None, dv=None, workspace=None,
-             stream=None):
+             stream=None, deterministic: bool = False):
     """dQ, dK, dV = recompute-based attention backward (fa_backward; fa_backward_gqa when k, v
-    have fewer heads than q)."""
+    have fewer heads than q; fa_backward_deterministic, bit-reproducible, when asked)."""
     B, H, N, d, Hkv = _check_qkv(q, k, v)
     for name, t in (("o", o), ("do", do)):
         if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
@@ -192,12 +201,18 @@ def backward(q, k, v, o, lse, do, *, causal: bool = False, scale: Optional[float
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    need = backward_workspace_size(B, H, N, d)
+    need = (backward_deterministic_workspace_size(B, H, N) if deterministic
+            else backward_workspace_size(B, H, N, d))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv))
     tail = (d, scale, int(bool(causal)), _ptr(block_mask), _DTYPES[q.dtype], _ptr(kv_lens),
             _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if deterministic:
+        st = lib.fa_backward_deterministic(*args, B, H, Hkv, N, *tail)
+        if st != FA_OK:
+            raise FaError(st, "fa_backward_deterministic")
+        return dq, dk, dv
     if Hkv == H:
         st = lib.fa_backward(*args, B, H, N, *tail)
     else:

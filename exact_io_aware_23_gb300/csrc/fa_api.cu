@@ -204,6 +204,11 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d) {
   return round_up(rows * (size_t)d * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
 }
 
+size_t fa_backward_deterministic_workspace_size(int B, int H, int N) {
+  if (B <= 0 || H <= 0 || N <= 0) return 0;
+  return round_up((size_t)B * H * N * sizeof(float), 256);   // D only: no dQ accumulator
+}
+
 }  // extern "C"
 
 namespace {
@@ -212,11 +217,13 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
                         const void* dO, const float* lse, void* dq, void* dk, void* dv,
                         int B, int H, int Hkv, int N, int d, float scale, int causal,
                         const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+                        void* workspace, size_t workspace_bytes, void* stream,
+                        bool deterministic) {
   fa_status st = check_common(B, H, N, d, scale, dtype);
   if (st != FA_OK) return st;
   st = check_heads(H, Hkv, dtype);
   if (st != FA_OK) return st;
+  if (deterministic && dtype == FA_FP32) return FA_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0) return FA_OK;
   if (block_mask != nullptr && N > kMaxBlockSparseN) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace)
@@ -225,13 +232,21 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
       !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
-  if (workspace_bytes < fa_backward_workspace_size(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  const size_t need = deterministic ? fa_backward_deterministic_workspace_size(B, H, N)
+                                    : fa_backward_workspace_size(B, H, N, d);
+  if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.o = o; a.dO = dO; a.lse = lse; a.dq = dq; a.dk = dk; a.dv = dv;
   const size_t rows = (size_t)B * H * N;
-  a.dq_acc = static_cast<float*>(workspace);
-  a.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                     round_up(rows * (size_t)d * sizeof(float), 256));
+  if (deterministic) {
+    a.dq_acc = nullptr;
+    a.delta = static_cast<float*>(workspace);
+  } else {
+    a.dq_acc = static_cast<float*>(workspace);
+    a.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       round_up(rows * (size_t)d * sizeof(float), 256));
+  }
+  a.deterministic = deterministic ? 1 : 0;
   a.B = B; a.H = H; a.Hkv = Hkv; a.N = N; a.d = d; a.scale = scale; a.causal = causal != 0;
   a.block_mask = block_mask; a.n_tiles = (N + fa::kMaskTile - 1) / fa::kMaskTile;
   a.kv_lens = kv_lens; a.dbg = knobs();
@@ -243,7 +258,8 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
   cudaError_t e = fa::launch_bwd_preprocess(a, dtype, s);
   if (e == cudaSuccess)
     e = dtype == FA_FP32 ? fa::launch_bwd_simt(a, dtype, s) : fa::launch_bwd_sm103(a, dtype, s);
-  if (e == cudaSuccess) e = fa::launch_bwd_dq_convert(a, dtype, s);
+  if (e == cudaSuccess)
+    e = deterministic ? fa::launch_dq_sm103(a, dtype, s) : fa::launch_bwd_dq_convert(a, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -257,7 +273,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                       const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
                       void* workspace, size_t workspace_bytes, void* stream) {
   return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, N, d, scale, causal, block_mask,
-                       dtype, kv_lens, workspace, workspace_bytes, stream);
+                       dtype, kv_lens, workspace, workspace_bytes, stream, false);
 }
 
 fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const void* o,
@@ -266,7 +282,17 @@ fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const voi
                           const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
                           void* workspace, size_t workspace_bytes, void* stream) {
   return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal, block_mask,
-                       dtype, kv_lens, workspace, workspace_bytes, stream);
+                       dtype, kv_lens, workspace, workspace_bytes, stream, false);
+}
+
+fa_status fa_backward_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                    const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                                    int B, int H, int Hkv, int N, int d, float scale, int causal,
+                                    const uint8_t* block_mask, fa_dtype dtype,
+                                    const int32_t* kv_lens, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal, block_mask,
+                       dtype, kv_lens, workspace, workspace_bytes, stream, true);
 }
 
 fa_status fa_check_device_status(void* stream) {

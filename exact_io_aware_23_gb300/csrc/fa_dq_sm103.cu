@@ -1,0 +1,423 @@
+// dQ pass of the deterministic attention backward for sm_103a (bf16 or fp16 in, fp32 accumulate),
+// d in {64, 128}.
+//
+// The backward recomputes P from the stored per-row statistic ("FlashAttention paper story",
+// backward paragraph; "FlashAttention: Exact Attention with Less GPU Memory", "Tiling, and
+// paying arithmetic to avoid memory").  For dQ of one query row i:
+//     P_ij = exp(scale*S_ij - LSE_i),  dP_ij = dO_i . V_j,  dS_ij = P_ij (dP_ij - D_i),
+//     dQ_i = scale * sum_j dS_ij K_j.
+// The key-stationary kernel (fa_bwd_sm103.cu) adds each key tile's share of dQ into an fp32
+// workspace from many CTAs at once, so the order of the additions (and the last bits of dQ)
+// depends on scheduling.  Here one CTA owns a 128-row query tile and visits its live key tiles in
+// ascending order, accumulating dQ in TMEM: the result is the same bits on every run.  The cost
+// is recomputing S and dP (two more products per tile pair than the fused kernel spends on dQ).
+//
+// GB300 design: one CTA per 128-row query tile of one (b, h) slice, 320 threads.
+//   warp 8      TMA producer: Q_i and dO_i once; K_j, V_j through a ring of stages.
+//   warp 9      MMA issuer: S = Q_i K_j^T into one of two S buffers (SS); dQ += dS K_{j-1}
+//               for the previous tile (TS: dS read from TMEM, K MN-major in shared memory),
+//               then dP = dO_i V_j^T (SS).  The tensor pipe runs the next tile's S while the
+//               compute warps work on this one.
+//   warps 0-7   two warpgroups over the tile's keys [0,64) and [64,128); thread = query row =
+//               TMEM lane.  P from S (exp2 of scale*log2e*S - LSE*log2e), dS = P (dP - D)
+//               packed to bf16/fp16 pairs into the first 32 columns of the warpgroup's own
+//               64 S columns (no other warp reads them).  At the end each warpgroup converts
+//               half of dQ's columns and stores them.
+//   TMEM: dQ [0,128) (d columns used), S buffers [128,256) and [256,384), dP [384,512).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "fa_internal.cuh"
+#include "fa_sm103.cuh"
+#include "ptx_sm103.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int BM = 128;          // query rows per CTA
+constexpr int BN = 128;          // keys per tile
+constexpr int kThreads = 320;
+constexpr int kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D, bool F16>
+struct Cfg {
+  static constexpr int kTile = 128 * D * 2;                  // one 128-row operand tile
+  static constexpr int kStages = D == 64 ? 4 : 2;            // K/V ring
+  static constexpr int kQ = 0;
+  static constexpr int kDO = kQ + kTile;
+  static constexpr int kKV = kDO + kTile;                    // stage s: K at kKV + 2s*kTile, V next
+  static constexpr int kBar = kKV + kStages * 2 * kTile;
+  static constexpr int kSmem = kBar + 256;
+  static constexpr uint32_t kDQ = 0, kS = 128, kDP = 384;    // TMEM columns; S buffer b at kS + 128b
+  static constexpr uint32_t kIdescS = ptx::idesc_f32acc(128, 128, false, false, F16);  // S, dP
+  static constexpr uint32_t kIdescDQ = ptx::idesc_f32acc(128, D, false, true, F16);    // dQ
+};
+
+struct Bars {             // at most 128 bytes (the live-tile bitmap follows)
+  uint64_t q_full;
+  uint64_t kv_full[4];
+  uint64_t kv_empty[4];
+  uint64_t s_full[2];
+  uint64_t dp_full;
+  uint64_t ds_ready;
+  uint64_t dq_done;
+  uint32_t tmem_base;
+};
+
+static_assert(sizeof(Bars) <= 128, "the live-tile bitmap starts 128 bytes after the barriers");
+
+enum : int { kNone = 0, kPartial = 1, kFull = 2 };
+
+// Key tiles of one query tile: [0, j_end) bounded by the causal diagonal and the valid key
+// length; a tile mask removes more (then `bits` lists the live ones).
+struct Geo {
+  int i, q0, N, kv_lim, causal, T, j_end;
+  const uint8_t* bm;
+  const uint32_t* bits;
+  __device__ int kind(int j) const {
+    const int r0 = q0, r1 = min(q0 + BM, N) - 1;
+    const int c0 = j * BN, c1 = c0 + BN - 1;
+    if (bm != nullptr && bm[(size_t)i * T + j] == 0) return kNone;
+    if (c0 >= kv_lim || (causal && c0 > r1)) return kNone;
+    if (c1 < kv_lim && (!causal || c1 <= r0)) return kFull;
+    return kPartial;
+  }
+  __device__ int next(int j) const {
+    if (bits == nullptr) return j;
+    while (j < j_end) {
+      const uint32_t w = bits[j >> 5] >> (j & 31);
+      if (w != 0u) return min(j + __ffs(w) - 1, j_end);
+      j = (j | 31) + 1;
+    }
+    return j_end;
+  }
+};
+
+template <int D, bool F16>
+__global__ void __launch_bounds__(kThreads, 1)
+dq_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                BwdArgs a) {
+  using C = Cfg<D, F16>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if ((ptx::smem_u32(smem) & 1023u) != 0) {      // the operand tiles need 1 KB alignment
+    if (threadIdx.x == 0) atomicExch(a.err, 2);
+    return;
+  }
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kBar);
+  const uint32_t sbase = ptx::smem_u32(smem);
+  // Work order: with masks the (b, h) slice varies fastest and, when causal, the longest query
+  // tiles (the last ones) start first; without, one slice's tiles run together and share its
+  // K/V stream in L2.
+  const int BH = a.B * a.H;
+  const int n_qt = (a.N + BM - 1) / BM;
+  const int bh = a.heads_fastest ? (int)(blockIdx.x % BH) : (int)(blockIdx.x / n_qt);
+  const int it = a.heads_fastest ? (int)(blockIdx.x / BH) : (int)(blockIdx.x % n_qt);
+  const int b = bh / a.H;
+  // grouped-query attention: query head h reads key/value head h / (H / Hkv)
+  const int bh_kv = b * a.Hkv + (bh % a.H) / (a.H / a.Hkv);
+  const uint32_t lim_ms = a.dbg.wait_limit_ms;
+
+  Geo g;
+  g.i = a.causal ? n_qt - 1 - it : it;
+  g.q0 = g.i * BM;
+  g.N = a.N;
+  int kvl = a.N;
+  if (a.kv_lens != nullptr) kvl = max(0, min(a.N, (int)a.kv_lens[b]));
+  g.kv_lim = kvl;
+  g.causal = a.causal;
+  g.T = a.n_tiles;
+  g.bm = a.block_mask;
+  g.j_end = (kvl + BN - 1) / BN;
+  if (a.causal) g.j_end = min(g.j_end, g.i + 1);
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->kv_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[s]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bars->s_full[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->s_full[1]), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->ds_ready), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->dq_done), 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  g.bits = nullptr;
+  if (a.block_mask != nullptr) {                 // live-tile bitmap, one ballot per 32 tiles
+    uint32_t* live_bits = reinterpret_cast<uint32_t*>(smem + C::kBar + 128);
+    g.bits = live_bits;
+    for (int w = warp; w < (g.j_end + 31) / 32; w += kThreads / 32) {
+      const int j = w * 32 + lane;
+      const uint32_t word = __ballot_sync(0xffffffffu, j < g.j_end && g.kind(j) != kNone);
+      if (lane == 0) live_bits[w] = word;
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const bool any = g.next(0) < g.j_end;
+
+  if (warp == 8) {
+    // ------------------------------- TMA producer -----------------------------------------------
+    if (lane == 0 && any) {
+      bool ok = true;
+      int n = 0;
+      const uint32_t qb = ptx::smem_u32(&bars->q_full);
+      ptx::mbar_arrive_expect_tx(qb, 2 * C::kTile);
+      for (int hh = 0; hh < D / 64; ++hh) {
+        ptx::tma_load_3d(sbase + C::kQ + hh * 128 * 128, &tmQ, qb, hh * 64, g.q0, bh);
+        ptx::tma_load_3d(sbase + C::kDO + hh * 128 * 128, &tmDO, qb, hh * 64, g.q0, bh);
+      }
+      for (int j = g.next(0); j < g.j_end && ok; j = g.next(j + 1), ++n) {
+        const int stg = n % C::kStages;
+        const uint32_t ph = (uint32_t)(n / C::kStages) & 1u;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[stg]), ph ^ 1u, lim_ms, a.err);
+        if (!ok) break;
+        const uint32_t fb = ptx::smem_u32(&bars->kv_full[stg]);
+        ptx::mbar_arrive_expect_tx(fb, 2 * C::kTile);
+        const uint32_t sk = sbase + C::kKV + stg * 2 * C::kTile;
+        for (int hh = 0; hh < D / 64; ++hh) {
+          ptx::tma_load_3d(sk + hh * 128 * 128, &tmK, fb, hh * 64, j * BN, bh_kv);
+          ptx::tma_load_3d(sk + C::kTile + hh * 128 * 128, &tmV, fb, hh * 64, j * BN, bh_kv);
+        }
+      }
+      // drain: copies in flight must land before shared memory is released
+      ptx::mbar_wait(qb, 0, lim_ms, a.err);
+      for (int m = max(0, n - C::kStages); m < n; ++m)
+        ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[m % C::kStages]), (uint32_t)(m / C::kStages) & 1u,
+                       lim_ms, a.err);
+    }
+  } else if (warp == 9) {
+    // ------------------------------- MMA issuer -------------------------------------------------
+    if (lane == 0) {
+      bool ok = true;
+      int n = 0, prev_stg = 0;
+      // dQ += dS(m) K(m): A = dS packed in S buffer m&1 (keys 64w..64w+63 in its columns
+      // 64w..64w+31), B = K_m with the key index as K (MN-major, 16 keys = 2048 bytes a step)
+      auto dq_mma = [&](int m, int stg) {
+        const uint32_t sb = C::kS + (uint32_t)(m & 1) * 128;
+        const uint32_t sk = sbase + C::kKV + stg * 2 * C::kTile;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          ptx::mma_ts(tmem + C::kDQ, tmem + sb + (kk / 4) * 64 + (kk % 4) * 8,
+                      ptx::sdesc_sw128(sk + kk * 2048, 128 * 128, 1024), C::kIdescDQ,
+                      (m > 0 || kk > 0) ? 1u : 0u);
+      };
+      if (any) {
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, lim_ms, a.err);
+        for (int j = g.next(0); j < g.j_end && ok; j = g.next(j + 1), ++n) {
+          const int stg = n % C::kStages;
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[stg]), (uint32_t)(n / C::kStages) & 1u,
+                              lim_ms, a.err);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint32_t sk = sbase + C::kKV + stg * 2 * C::kTile;
+          // S(n) = Q K_j^T (K-major operands, k-steps of 16 along d).  Its buffer last held
+          // dS(n-2), read by dQ(n-2), which was issued before this.
+          const uint32_t sb = C::kS + (uint32_t)(n & 1) * 128;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+            ptx::mma_ss(tmem + sb, ptx::sdesc_sw128(sbase + C::kQ + off, 16, 1024),
+                        ptx::sdesc_sw128(sk + off, 16, 1024), C::kIdescS, kk > 0);
+          }
+          ptx::mma_commit(ptx::smem_u32(&bars->s_full[n & 1]));
+          if (n > 0) {
+            // tile n-1 done by the compute warps: dS(n-1) is in TMEM and dP(n-1) has been read
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_ready), (uint32_t)(n - 1) & 1u, lim_ms, a.err);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            dq_mma(n - 1, prev_stg);
+            ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[prev_stg]));
+          }
+          // dP(n) = dO V_j^T
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+            ptx::mma_ss(tmem + C::kDP, ptx::sdesc_sw128(sbase + C::kDO + off, 16, 1024),
+                        ptx::sdesc_sw128(sk + C::kTile + off, 16, 1024), C::kIdescS, kk > 0);
+          }
+          ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
+          prev_stg = stg;
+        }
+        if (ok && n > 0) {
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_ready), (uint32_t)(n - 1) & 1u, lim_ms, a.err);
+          if (ok) {
+            ptx::tc_fence_after();
+            dq_mma(n - 1, prev_stg);
+            ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[prev_stg]));
+          }
+        }
+      }
+      ptx::mma_commit(ptx::smem_u32(&bars->dq_done));
+      ptx::mbar_wait(ptx::smem_u32(&bars->dq_done), 0, lim_ms, a.err);
+    }
+  } else {
+    // ------------------------------- compute warpgroups -----------------------------------------
+    const int wg = warp / 4, sub = warp % 4;
+    const int r = sub * 32 + lane;                   // query row within the tile (TMEM lane)
+    const int q = g.q0 + r;
+    const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
+    const float c = a.scale * kLog2e;
+    const float2 c2 = make_float2(c, c);
+    const size_t row = (size_t)bh * a.N + q;
+    float L = q < a.N ? a.lse[row] : -INFINITY;
+    const float nl = L == -INFINITY ? -INFINITY : -L * kLog2e;   // P vanishes on empty rows
+    const float2 nl2 = make_float2(nl, nl);
+    const float dd = q < a.N ? a.delta[row] : 0.f;
+    const float2 dd2 = make_float2(dd, dd);
+    bool ok = true;
+    int n = 0;
+    for (int j = g.next(0); j < g.j_end; j = g.next(j + 1), ++n) {
+      const int kind = g.kind(j);
+      const int k0 = j * BN + wg * 64;              // first key of this warpgroup's columns
+      const uint32_t sb = C::kS + (uint32_t)(n & 1) * 128 + wg * 64;
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[n & 1]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      float p[64];
+      {
+        uint32_t raw[2][32];
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) ptx::tmem_ld32(tmem + lane_off + sb + hc * 32, raw[hc]);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          ptx::reg_fence(raw[hc]);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int col = hc * 32 + e;
+            const float2 x = ptx::fma2(make_float2(__uint_as_float(raw[hc][e]), __uint_as_float(raw[hc][e + 1])),
+                                       c2, nl2);
+            float v0 = ptx::ex2(x.x), v1 = ptx::ex2(x.y);
+            if (kind == kPartial) {
+              const int key = k0 + col;
+              v0 = (key < g.kv_lim && (!g.causal || key <= q)) ? v0 : 0.f;
+              v1 = (key + 1 < g.kv_lim && (!g.causal || key + 1 <= q)) ? v1 : 0.f;
+            }
+            p[col] = v0;
+            p[col + 1] = v1;
+          }
+        }
+      }
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->dp_full), (uint32_t)n & 1u, lim_ms, a.err);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      {
+        uint32_t raw[2][32];
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) ptx::tmem_ld32(tmem + lane_off + C::kDP + wg * 64 + hc * 32, raw[hc]);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          ptx::reg_fence(raw[hc]);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int col = hc * 32 + e;
+            const float2 dpd = ptx::sub2(make_float2(__uint_as_float(raw[hc][e]), __uint_as_float(raw[hc][e + 1])),
+                                         dd2);
+            const float2 ds = ptx::mul2(make_float2(p[col], p[col + 1]), dpd);
+            p[col] = ds.x;
+            p[col + 1] = ds.y;
+          }
+        }
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
+        ptx::tmem_st32(tmem + lane_off + sb, pk);
+        ptx::tmem_wait_st();
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_ready));
+    }
+    // ------------------------------- epilogue: dQ = scale * acc, this warpgroup's half of d -----
+    const bool have = ok && n > 0;
+    if (have) {
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->dq_done), 0, lim_ms, a.err);
+      ptx::tc_fence_after();
+    }
+    uint16_t* out = static_cast<uint16_t*>(a.dq) + row * D + wg * (D / 2);
+#pragma unroll 1
+    for (int hc = 0; hc < D / 64; ++hc) {
+      uint32_t raw[32];
+      if (have && ok) {
+        ptx::tmem_ld32(tmem + lane_off + C::kDQ + wg * (D / 2) + hc * 32, raw);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(raw);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) raw[e] = 0u;
+      }
+      if (q < a.N) {
+        uint4* dst = reinterpret_cast<uint4*>(out + hc * 32);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          uint4 w;
+          w.x = ptx::pack2<F16>(__uint_as_float(raw[8 * v4 + 0]) * a.scale, __uint_as_float(raw[8 * v4 + 1]) * a.scale);
+          w.y = ptx::pack2<F16>(__uint_as_float(raw[8 * v4 + 2]) * a.scale, __uint_as_float(raw[8 * v4 + 3]) * a.scale);
+          w.z = ptx::pack2<F16>(__uint_as_float(raw[8 * v4 + 4]) * a.scale, __uint_as_float(raw[8 * v4 + 5]) * a.scale);
+          w.w = ptx::pack2<F16>(__uint_as_float(raw[8 * v4 + 6]) * a.scale, __uint_as_float(raw[8 * v4 + 7]) * a.scale);
+          dst[v4] = w;
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 9) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH, bool f16) {
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_tensor_map(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                           3, base, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int D, bool F16>
+cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
+  CUtensorMap mq, mk, mv, mdo;
+  const int BH = a.B * a.H;            // query slices (Q, dO, dQ)
+  const int BHkv = a.B * a.Hkv;        // key/value slices (K, V)
+  cudaError_t e;
+  if ((e = make_map(&mq, a.q, D, a.N, BH, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, a.k, D, a.N, BHkv, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.v, D, a.N, BHkv, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mdo, a.dO, D, a.N, BH, F16)) != cudaSuccess) return e;
+  auto kern = dq_sm103_kernel<D, F16>;
+  // barriers (128 bytes) + the live-tile bitmap of a block-sparse mask (one bit per key tile)
+  int smem = Cfg<D, F16>::kSmem;
+  if (a.block_mask != nullptr) smem = max(smem, Cfg<D, F16>::kBar + 128 + ((a.n_tiles + 127) / 128) * 16);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(((a.N + BM - 1) / BM) * BH);
+  kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mdo, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dq_sm103(const BwdArgs& a, fa_dtype dt, cudaStream_t s) {
+  if (dt == FA_FP16) return a.d == 64 ? launch<64, true>(a, s) : launch<128, true>(a, s);
+  return a.d == 64 ? launch<64, false>(a, s) : launch<128, false>(a, s);
+}
+
+}  // namespace fa

@@ -65,7 +65,7 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  float* dq_acc;    // workspace: fp32 [B, H, N, d]
+  float* dq_acc;    // workspace: fp32 [B, H, N, d]; null in the deterministic backward
   float* delta;     // workspace: fp32 [B, H, N], D_i = rowsum(dO_i * O_i)
   int B, H, N, d;
   int Hkv;          // key/value heads (K, V, dK, dV are [B, Hkv, N, d])
@@ -77,14 +77,17 @@ struct BwdArgs {
   int* err;
   DebugKnobs dbg;
   int heads_fastest;          // launch order: (b, h) slice fastest (unequal work per tile)
+  // Deterministic backward: the key-stationary kernel produces dK and dV only, and a separate
+  // query-stationary kernel produces dQ with no cross-CTA accumulation.
+  int deterministic;
 };
 
 // CUDA-core (SIMT) kernels: the fp32 path.
 cudaError_t launch_fwd_simt(const FwdArgs& a, fa_dtype dt, cudaStream_t s);
 cudaError_t launch_bwd_simt(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
 
-// Shared backward pieces: D = rowsum(dO * O) with dQ accumulator zeroing, and the final dQ
-// scale + convert.
+// Shared backward pieces: D = rowsum(dO * O) with dQ accumulator zeroing (when there is an
+// accumulator), and the final dQ scale + convert.
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
 

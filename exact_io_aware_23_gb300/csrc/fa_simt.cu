@@ -300,7 +300,8 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(BwdArgs a) {
   }
 }
 
-// D_i = sum_c dO_ic * O_ic (O as stored), and zero row i of the dQ accumulator.  One warp/row.
+// D_i = sum_c dO_ic * O_ic (O as stored), and zero row i of the dQ accumulator if there is one.
+// One warp per row.
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) bwd_preprocess_kernel(BwdArgs a) {
   const size_t rows = (size_t)a.B * a.H * a.N;
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(kThreads) bwd_preprocess_kernel(BwdArgs a) {
 #pragma unroll
   for (int c = lane; c < D; c += 32) {
     acc = fmaf(to_f<T>(dO[c]), to_f<T>(o[c]), acc);
-    a.dq_acc[row * D + c] = 0.f;
+    if (a.dq_acc != nullptr) a.dq_acc[row * D + c] = 0.f;
   }
   acc = warp_sum(acc);
   if (lane == 0) a.delta[row] = acc;

@@ -99,6 +99,25 @@ fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const voi
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Deterministic backward: the same gradients as fa_backward_gqa (Hkv = H for plain multi-head
+ * attention), reproducible to the bit from run to run on the same GPU and inputs.  The
+ * recompute-based backward ("FlashAttention paper story", backward paragraph) is split into a
+ * pass over key tiles that writes dK and dV, and a pass over query tiles that recomputes S and
+ * dP and accumulates each dQ row in one place in a fixed key order; no partial sums are added
+ * from several CTAs.  It costs two extra matrix products per tile pair.  bf16 or fp16 only
+ * (FA_ERR_UNSUPPORTED for fp32).  workspace: at least
+ * fa_backward_deterministic_workspace_size(B, H, N) bytes, 256-byte aligned, caller-owned,
+ * contents on entry irrelevant.  Other arguments, errors and ownership as in fa_backward.
+ */
+size_t fa_backward_deterministic_workspace_size(int B, int H, int N);
+fa_status fa_backward_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                    const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                                    int B, int H, int Hkv, int N, int d, float scale, int causal,
+                                    const uint8_t* block_mask, fa_dtype dtype,
+                                    const int32_t* kv_lens, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/*
  * Split-KV forward for decode-shaped problems (few queries against a long key sequence) and for
  * problems with too few (b, h) slices to fill the GPU: the key tiles of every query tile are cut
  * into n_splits ranges processed by separate CTAs, each producing its own (O_s, LSE_s); a merge
@@ -142,7 +161,8 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d);
  *                 256-byte aligned, owned by the caller; its contents on entry do not matter
  *                 and are overwritten.  Two calls in flight at once need two workspaces.
  * Other arguments as in fa_forward.  The result of concurrent dQ accumulation is
- * nondeterministic in the last bits (fp32 atomic add order).
+ * nondeterministic in the last bits (the order of the fp32 additions into the dQ accumulator
+ * varies); fa_backward_deterministic is the reproducible variant.
  */
 fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
                       const void* dO, const float* lse, void* dq, void* dk, void* dv,

@@ -36,14 +36,14 @@ def _dev(x):
     return q, k, v, do, dict(causal=x["causal"], scale=x["scale"], block_mask=bm, kv_lens=kl)
 
 
-def run_gpu(x, backward=True):
+def run_gpu(x, backward=True, deterministic=False):
     """Chained GPU forward (and backward on the forward's own O, LSE)."""
     import exact_io_aware_23_gb300 as fa
     q, k, v, do, kw = _dev(x)
     o, lse = fa.forward(q, k, v, **kw)
     out = dict(o=o, lse=lse)
     if backward:
-        dq, dk, dv = fa.backward(q, k, v, o, lse, do, **kw)
+        dq, dk, dv = fa.backward(q, k, v, o, lse, do, deterministic=deterministic, **kw)
         out.update(dq=dq, dk=dk, dv=dv)
     assert fa.check_device_status() == 0
     return out
@@ -103,7 +103,7 @@ def compare(x, out, heads=None, rows=None, backward=True):
     return res
 
 
-def check_backward_given_o(x):
+def check_backward_given_o(x, deterministic=False):
     """GPU backward on the oracle's O (rounded to the working dtype) and LSE, against the
     oracle's backward for that O; forward checked separately."""
     import exact_io_aware_23_gb300 as fa
@@ -113,6 +113,7 @@ def check_backward_given_o(x):
     lse_in = torch.from_numpy(L).to(torch.float32)
     q, k, v, do, kw = _dev(x)
     dev = q.device
-    dq, dk, dv = fa.backward(q, k, v, o_in.to(dev), lse_in.to(dev), do, **kw)
+    dq, dk, dv = fa.backward(q, k, v, o_in.to(dev), lse_in.to(dev), do, deterministic=deterministic,
+                             **kw)
     assert fa.check_device_status() == 0
     return compare_bwd(x, dict(dq=dq, dk=dk, dv=dv), o_given=o_in.to(torch.float64).numpy())

@@ -147,3 +147,27 @@ def test_gqa_argument_checks(lib):
         assert call(dtype=2, N=0) == OK
     assert fwd_g(q=None) == INVALID
     assert bwd_g(wsb=ws - 4) == INVALID
+
+
+def test_deterministic_backward_argument_checks(lib):
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_backward_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f,
+                                              i, vp, i, vp, vp, sz, vp]
+    lib.fa_backward_deterministic_workspace_size.argtypes = [i, i, i]
+    lib.fa_backward_deterministic_workspace_size.restype = sz
+    ws = lib.fa_backward_deterministic_workspace_size(2, 8, 100)
+    assert ws % 256 == 0 and ws >= 2 * 8 * 100 * 4
+    assert ws < lib.fa_backward_workspace_size(2, 8, 100, 64)      # no dQ accumulator
+    assert lib.fa_backward_deterministic_workspace_size(0, 8, 100) == 0
+
+    def call(Hkv=8, N=100, dtype=0, wsb=ws, w=P, d=64):
+        return lib.fa_backward_deterministic(P, P, P, P, P, P, P, P, P, 2, 8, Hkv, N, d, 0.125, 1,
+                                             None, dtype, None, w, wsb, None)
+    assert call(dtype=1) == UNSUPPORTED          # fp32: the SIMT backward has no such variant
+    assert call(d=96) == UNSUPPORTED
+    assert call(Hkv=3) == UNSUPPORTED
+    assert call(Hkv=0) == INVALID
+    assert call(w=None) == INVALID
+    assert call(w=ctypes.c_void_p(0x10010)) == INVALID
+    assert call(wsb=ws - 4) == INVALID
+    assert call(N=0) == OK
