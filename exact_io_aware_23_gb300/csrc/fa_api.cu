@@ -256,10 +256,14 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
   if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = fa::launch_bwd_preprocess(a, dtype, s);
-  if (e == cudaSuccess)
-    e = dtype == FA_FP32 ? fa::launch_bwd_simt(a, dtype, s) : fa::launch_bwd_sm103(a, dtype, s);
-  if (e == cudaSuccess)
-    e = deterministic ? fa::launch_dq_sm103(a, dtype, s) : fa::launch_bwd_dq_convert(a, dtype, s);
+  if (e == cudaSuccess) {
+    if (deterministic) {
+      e = fa::launch_bwd_split_sm103(a, dtype, s);
+    } else {
+      e = dtype == FA_FP32 ? fa::launch_bwd_simt(a, dtype, s) : fa::launch_bwd_sm103(a, dtype, s);
+      if (e == cudaSuccess) e = fa::launch_bwd_dq_convert(a, dtype, s);
+    }
+  }
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -27,16 +27,10 @@
 //               X[0,64), dS^T packed in Y[0,64); once dK has read dS^T, the two dQ halves go to
 //               Y[0,64) and Y[64,128), so the next tile's S^T (into X) overlaps the dQ drain.
 //   TMEM d=64:  dV [0,64) dK [64,128) X [128,256) Y [256,384) dQ [384,448).
-//
-// The deterministic backward instantiates this kernel without dQ (kDQ = false): no dS staging,
-// no dQ products or reductions; each Q/dO stage is handed back to the producer by the MMA
-// commit that follows the tile's dK product.  dQ then comes from the query-stationary kernel
-// in fa_dq_sm103.cu.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
-#include <string.h>
 
 #include "fa_internal.cuh"
 #include "fa_sm103.cuh"
@@ -116,7 +110,7 @@ struct Geo {
   }
 };
 
-template <int D, bool F16, bool kDQ>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -161,7 +155,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     ptx::mbar_init(ptx::smem_u32(&bars->kv_full), 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->st_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->st_empty[s]), kDQ ? 8 : 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->st_empty[s]), 8);
     }
     ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
@@ -263,7 +257,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                         ptx::sdesc_sw128(sq + off, 16, 1024), C::kIdescST, kk > 0);
           }
           ptx::mma_commit(ptx::smem_u32(&bars->s_full));
-          if (kDQ && n > 0 && D == 128) {   // Y holds the previous tile's dQ until it is drained
+          if (n > 0 && D == 128) {     // Y holds the previous tile's dQ until it is drained
             ok = ptx::mbar_wait(ptx::smem_u32(&bars->dq_free), (n - 1) & 1, lim_ms, a.err);
             if (!ok) break;
             ptx::tc_fence_after();
@@ -288,7 +282,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                         (n > 0 || kk > 0) ? 1u : 0u);
           // dK += dS^T Q once dS^T is ready
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_ready), n & 1, lim_ms, a.err);
-          if (kDQ && ok && n > 0 && D == 64)
+          if (ok && n > 0 && D == 64)
             ok = ptx::mbar_wait(ptx::smem_u32(&bars->dq_free), (n - 1) & 1, lim_ms, a.err);
           if (!ok) break;
           ptx::tc_fence_after();
@@ -297,11 +291,6 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             ptx::mma_ts(tmem + C::kDK, tmem + C::kY + kk * 8,
                         ptx::sdesc_sw128(sq + kk * 2048, 128 * 128, 1024), C::kIdescAcc,
                         (n > 0 || kk > 0) ? 1u : 0u);
-          if constexpr (!kDQ) {
-            // Q_i and dO_i are no longer read once dK's product is done
-            ptx::mma_commit(ptx::smem_u32(&bars->st_empty[st]));
-            continue;
-          }
           // dQ_i = dS K_j, 64 columns of d per part: A = dS (queries x keys, query-major in
           // shared memory), B = K (keys x d, d-major); 16 keys = 2048 bytes per step.
 #pragma unroll
@@ -385,7 +374,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_ready));
-        if (kDQ && lane == 0 && pend_st >= 0) {       // previous tile's staged dQ has been read
+        if (lane == 0 && pend_st >= 0) {              // previous tile's staged dQ has been read
           ptx::bulk_wait_read0();
           ptx::mbar_arrive(ptx::smem_u32(&bars->st_empty[pend_st]));
           pend_st = -1;
@@ -426,22 +415,19 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 32; ++e) pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
         ptx::tmem_st32(tmem + lane_off + C::kY + wg * 32, pk);
-        if constexpr (kDQ) {
-          // dS into shared memory, query-major 128-byte-swizzled: row = key, 64 queries per atom
-          uint8_t* row = smem + C::kDS + wg * (128 * 128) + kr * 128;
+        // dS into shared memory, query-major 128-byte-swizzled: row = key, 64 queries per atom
+        uint8_t* row = smem + C::kDS + wg * (128 * 128) + kr * 128;
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            uint4 w = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            *reinterpret_cast<uint4*>(row + ((ch ^ (kr & 7)) << 4)) = w;
-          }
+        for (int ch = 0; ch < 8; ++ch) {
+          uint4 w = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          *reinterpret_cast<uint4*>(row + ((ch ^ (kr & 7)) << 4)) = w;
         }
       }
-      if constexpr (kDQ) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_ready));
-      if constexpr (!kDQ) continue;
       // dQ of this query tile: lane = query row; this warpgroup takes half of d, in boxes of 32
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->dq_full), n & 1, lim_ms, a.err);
       if (!ok) break;
@@ -484,7 +470,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         __syncwarp();
       }
     }
-    if (kDQ && lane == 0) {
+    if (lane == 0) {
       ptx::bulk_wait0();                              // every reduction has landed in global memory
       if (pend_st >= 0) ptx::mbar_arrive(ptx::smem_u32(&bars->st_empty[pend_st]));
     }
@@ -538,10 +524,9 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH, boo
                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int D, bool F16, bool kDQ>
+template <int D, bool F16>
 cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv, mdo, mdq;
-  memset(&mdq, 0, sizeof(mdq));           // not read without dQ
   const int BH = a.B * a.H;            // query slices (Q, dO, dQ)
   const int BHkv = a.B * a.Hkv;        // key/value slices (K, V, dK, dV)
   cudaError_t e;
@@ -549,7 +534,7 @@ cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
   if ((e = make_map(&mk, a.k, D, a.N, BHkv, F16)) != cudaSuccess) return e;
   if ((e = make_map(&mv, a.v, D, a.N, BHkv, F16)) != cudaSuccess) return e;
   if ((e = make_map(&mdo, a.dO, D, a.N, BH, F16)) != cudaSuccess) return e;
-  if (kDQ) {
+  {
     // fp32 dQ workspace viewed as (d, N, B*H); boxes of 32 columns x 32 rows
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.N, (cuuint64_t)BH};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)a.N * D * 4};
@@ -559,7 +544,7 @@ cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
                                estr, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
       return e;
   }
-  auto kern = bwd_sm103_kernel<D, F16, kDQ>;
+  auto kern = bwd_sm103_kernel<D, F16>;
   // barriers (128 bytes) + the live-tile bitmap of a block-sparse mask (one bit per query tile)
   int smem = Cfg<D, F16>::kSmem;
   if (a.block_mask != nullptr) smem = max(smem, Cfg<D, F16>::kBar + 128 + ((a.n_tiles + 127) / 128) * 16);
@@ -573,12 +558,8 @@ cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_bwd_sm103(const BwdArgs& a, fa_dtype dt, cudaStream_t s) {
-  if (a.deterministic) {
-    if (dt == FA_FP16) return a.d == 64 ? launch<64, true, false>(a, s) : launch<128, true, false>(a, s);
-    return a.d == 64 ? launch<64, false, false>(a, s) : launch<128, false, false>(a, s);
-  }
-  if (dt == FA_FP16) return a.d == 64 ? launch<64, true, true>(a, s) : launch<128, true, true>(a, s);
-  return a.d == 64 ? launch<64, false, true>(a, s) : launch<128, false, true>(a, s);
+  if (dt == FA_FP16) return a.d == 64 ? launch<64, true>(a, s) : launch<128, true>(a, s);
+  return a.d == 64 ? launch<64, false>(a, s) : launch<128, false>(a, s);
 }
 
 }  // namespace fa

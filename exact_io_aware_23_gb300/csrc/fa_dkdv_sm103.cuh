@@ -1,0 +1,462 @@
+// dK/dV pass of the deterministic attention backward for sm_103a (bf16 or fp16 in, fp32
+// accumulate), d in {64, 128}.
+//
+// The backward recomputes P from the stored per-row statistic ("FlashAttention paper story",
+// backward paragraph; "FlashAttention: Exact Attention with Less GPU Memory", "Tiling, and
+// paying arithmetic to avoid memory").  For one key tile j, over every live query tile i:
+//     P^T = exp(scale*S^T - LSE),  dV_j += P^T dO_i,  dP^T = V_j dO_i^T,
+//     dS^T = P^T * (dP^T - D),     dK_j += scale * dS^T Q_i.
+// dQ is left to the query-stationary kernel (fa_dq_sm103.cu), so nothing here is added from
+// several CTAs and the results do not depend on scheduling.
+//
+// GB300 design: one CTA per 128-key tile of one (b, h) key/value slice, 320 threads, visiting
+// every live query tile of every query head that reads the slice (one, or the G heads of a
+// group under grouped-query attention).  Key rows sit on the TMEM lanes: a thread owns one key.
+//   warp 8      TMA producer: K_j, V_j once; Q_i through a three-slot ring and dO_i through a
+//               two-slot ring (a Q tile is read until dK, a dO tile only until dV), and the
+//               tile's -LSE*log2(e) and D vectors through a two-slot ring in shared memory.
+//   warp 9      MMA issuer, one thread, in the order
+//                   dV += P^T(n) dO_n,  S^T(n+1) = K Q_{n+1}^T,  dK += dS^T(n) Q_n,
+//                   dP^T(n+1) = V dO_{n+1}^T
+//               so the tensor pipe computes the next tile's S^T while the compute warps build
+//               dS^T(n), and dK(n), dP^T(n+1) while they build P^T(n+1).
+//   warps 0-7   two warpgroups over the tile's query columns [0,64) and [64,128): P^T and dS^T
+//               in registers, packed to bf16/fp16 pairs into the first 32 columns of the
+//               warpgroup's own 64 columns of X and Y (no other warp reads those).
+//   TMEM: dV [0,d), dK [d,2d), X = S^T / P^T [2d, 2d+128), Y = dP^T / dS^T [2d+128, 2d+256).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "fa_internal.cuh"
+#include "fa_sm103.cuh"
+#include "ptx_sm103.cuh"
+
+namespace fa {
+namespace dkdv {
+
+constexpr int BM = 128;          // query rows per tile
+constexpr int BN = 128;          // keys per CTA
+constexpr int kThreads = 320;
+constexpr int kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D, bool F16>
+struct Cfg {
+  static constexpr int kTile = 128 * D * 2;                  // one 128-row operand tile
+  static constexpr int kQSlots = D == 64 ? 4 : 3;
+  static constexpr int kOSlots = D == 64 ? 4 : 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTile;
+  static constexpr int kQ = kV + kTile;                      // Q slot s at kQ + s*kTile
+  static constexpr int kO = kQ + kQSlots * kTile;            // dO slot s at kO + s*kTile
+  static constexpr int kVec = kO + kOSlots * kTile;          // vector slot s: lse2[128], delta[128]
+  static constexpr int kBar = kVec + 2 * 1024;
+  static constexpr int kSmem = kBar + 256;
+  static constexpr uint32_t kDV = 0, kDK = D, kX = 2 * D, kY = 2 * D + 128;   // TMEM columns
+  static constexpr uint32_t kIdescST = ptx::idesc_f32acc(128, 128, false, false, F16);  // S^T, dP^T
+  static constexpr uint32_t kIdescAcc = ptx::idesc_f32acc(128, D, false, true, F16);    // dV, dK
+};
+
+struct Bars {             // at most 256 bytes (the live-tile bitmap follows)
+  uint64_t kv_full;
+  uint64_t q_full[4];
+  uint64_t q_empty[4];
+  uint64_t o_full[4];
+  uint64_t o_empty[4];
+  uint64_t vec_empty[2];
+  uint64_t s_full;
+  uint64_t dp_full;
+  uint64_t p_ready;
+  uint64_t ds_ready;
+  uint64_t acc_done;
+  uint32_t tmem_base;
+};
+
+static_assert(sizeof(Bars) <= 256, "the live-tile bitmap starts 256 bytes after the barriers");
+
+enum : int { kNone = 0, kPartial = 1, kFull = 2 };
+
+// Query tiles of one key tile: [i_begin, i_end) bounded by the causal diagonal and the valid key
+// length; a tile mask removes more (then `bits` lists the live ones).
+struct Geo {
+  int k0, N, kv_lim, causal, T;
+  const uint8_t* bm;
+  int i_begin, i_end;
+  const uint32_t* bits;
+  __device__ int kind(int i) const {
+    const int r0 = i * BM, r1 = min(r0 + BM, N) - 1;
+    const int c0 = k0, c1 = k0 + BN - 1;
+    if (bm != nullptr && bm[(size_t)i * T + k0 / BN] == 0) return kNone;
+    if (c0 >= kv_lim || (causal && c0 > r1)) return kNone;
+    if (c1 < kv_lim && (!causal || c1 <= r0)) return kFull;
+    return kPartial;
+  }
+  __device__ int next(int i) const {
+    if (bits == nullptr) return i;
+    while (i < i_end) {
+      const uint32_t w = bits[i >> 5] >> (i & 31);
+      if (w != 0u) return min(i + __ffs(w) - 1, i_end);
+      i = (i | 31) + 1;
+    }
+    return i_end;
+  }
+};
+
+template <int D, bool F16>
+__device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                    const CUtensorMap& tmV, const CUtensorMap& tmDO,
+                                    const BwdArgs& a) {
+  using C = Cfg<D, F16>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if ((ptx::smem_u32(smem) & 1023u) != 0) {      // the operand tiles need 1 KB alignment
+    if (threadIdx.x == 0) atomicExch(a.err, 2);
+    return;
+  }
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kBar);
+  const uint32_t sbase = ptx::smem_u32(smem);
+  // Work order: with masks the key/value slice varies fastest, so every slice's heaviest key
+  // tiles (the first ones when causal) run in the first waves; without, one slice's key tiles
+  // run together and share its Q/dO stream in L2.
+  const int BH = a.B * a.Hkv;
+  const int n_kt = (a.N + BN - 1) / BN;
+  const int bh = a.heads_fastest ? unit % BH : unit / n_kt;   // K/V slice
+  const int jt = a.heads_fastest ? unit / BH : unit % n_kt;   // key tile
+  const int b = bh / a.Hkv;
+  const int G = a.H / a.Hkv;
+  const int bhq0 = b * a.H + (bh % a.Hkv) * G;   // first query slice of the group
+  const uint32_t lim_ms = a.dbg.wait_limit_ms;
+
+  Geo g;
+  g.k0 = jt * BN;
+  g.N = a.N;
+  int kvl = a.N;
+  if (a.kv_lens != nullptr) kvl = max(0, min(a.N, (int)a.kv_lens[b]));
+  g.kv_lim = kvl;
+  g.causal = a.causal;
+  g.T = a.n_tiles;
+  g.bm = a.block_mask;
+  g.i_begin = a.causal ? jt : 0;
+  g.i_end = g.k0 < g.kv_lim ? (a.N + BM - 1) / BM : 0;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bars->kv_full), 1);
+    for (int s = 0; s < C::kQSlots; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->q_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->q_empty[s]), 1);
+    }
+    for (int s = 0; s < C::kOSlots; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->o_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->o_empty[s]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bars->vec_empty[0]), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->vec_empty[1]), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->p_ready), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->ds_ready), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->acc_done), 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  g.bits = nullptr;
+  if (a.block_mask != nullptr) {                 // live-tile bitmap, one ballot per 32 tiles
+    uint32_t* live_bits = reinterpret_cast<uint32_t*>(smem + C::kBar + 256);
+    g.bits = live_bits;
+    for (int w = warp; w < (g.i_end + 31) / 32; w += kThreads / 32) {
+      const int i = w * 32 + lane;
+      const uint32_t word = __ballot_sync(0xffffffffu, i >= g.i_begin && i < g.i_end && g.kind(i) != kNone);
+      if (lane == 0) live_bits[w] = word;
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  int n_live = 0;                                // live query tiles of one head
+  for (int i = g.next(g.i_begin); i < g.i_end; i = g.next(i + 1)) ++n_live;
+  const int total = n_live * G;                  // tiles this CTA visits
+
+  if (warp == 8) {
+    // ------------------------------- producer (whole warp) --------------------------------------
+    if (total > 0) {
+      bool ok = true;
+      int n = 0;
+      if (lane == 0) {
+        const uint32_t kb = ptx::smem_u32(&bars->kv_full);
+        ptx::mbar_arrive_expect_tx(kb, 2 * C::kTile);
+        for (int hh = 0; hh < D / 64; ++hh) {
+          ptx::tma_load_3d(sbase + C::kK + hh * 128 * 128, &tmK, kb, hh * 64, g.k0, bh);
+          ptx::tma_load_3d(sbase + C::kV + hh * 128 * 128, &tmV, kb, hh * 64, g.k0, bh);
+        }
+      }
+      for (int hg = 0; hg < G && ok; ++hg)
+      for (int i = g.next(g.i_begin); i < g.i_end && ok; i = g.next(i + 1), ++n) {
+        const int bhq = bhq0 + hg;
+        const int qs = n % C::kQSlots, os = n % C::kOSlots, vs = n & 1;
+        if (lane == 0) {
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_empty[qs]), ((uint32_t)(n / C::kQSlots) & 1u) ^ 1u,
+                              lim_ms, a.err);
+          if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->vec_empty[vs]), ((uint32_t)(n >> 1) & 1u) ^ 1u,
+                                      lim_ms, a.err);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        // -LSE as a log2-domain bias (-inf where P must vanish) and D for the tile's rows
+        float* lse2 = reinterpret_cast<float*>(smem + C::kVec + vs * 1024);
+        float* dl = lse2 + 128;
+        for (int r = lane; r < 128; r += 32) {
+          const int q = i * BM + r;
+          const float L = q < a.N ? a.lse[(size_t)bhq * a.N + q] : -INFINITY;
+          lse2[r] = L == -INFINITY ? -INFINITY : -L * kLog2e;
+          dl[r] = q < a.N ? a.delta[(size_t)bhq * a.N + q] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t qb = ptx::smem_u32(&bars->q_full[qs]);
+          ptx::mbar_arrive_expect_tx(qb, C::kTile);
+          for (int hh = 0; hh < D / 64; ++hh)
+            ptx::tma_load_3d(sbase + C::kQ + qs * C::kTile + hh * 128 * 128, &tmQ, qb, hh * 64, i * BM, bhq);
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->o_empty[os]), ((uint32_t)(n / C::kOSlots) & 1u) ^ 1u,
+                              lim_ms, a.err);
+          if (ok) {
+            const uint32_t ob = ptx::smem_u32(&bars->o_full[os]);
+            ptx::mbar_arrive_expect_tx(ob, C::kTile);
+            for (int hh = 0; hh < D / 64; ++hh)
+              ptx::tma_load_3d(sbase + C::kO + os * C::kTile + hh * 128 * 128, &tmDO, ob, hh * 64, i * BM, bhq);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) { ++n; break; }
+      }
+      if (lane == 0) {   // drain: copies in flight must land before shared memory is released
+        ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, lim_ms, a.err);
+        for (int m = max(0, n - C::kQSlots); m < n; ++m)
+          ptx::mbar_wait(ptx::smem_u32(&bars->q_full[m % C::kQSlots]), (uint32_t)(m / C::kQSlots) & 1u,
+                         lim_ms, a.err);
+        for (int m = max(0, n - C::kOSlots); m < n; ++m)
+          ptx::mbar_wait(ptx::smem_u32(&bars->o_full[m % C::kOSlots]), (uint32_t)(m / C::kOSlots) & 1u,
+                         lim_ms, a.err);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------- MMA issuer -------------------------------------------------
+    if (lane == 0) {
+      // S^T = K Q^T into X, dP^T = V dO^T into Y (K-major operands, k-steps of 16 along d)
+      auto st_mma = [&](uint32_t dst, uint32_t src_kv, uint32_t src_q) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+          ptx::mma_ss(tmem + dst, ptx::sdesc_sw128(src_kv + off, 16, 1024),
+                      ptx::sdesc_sw128(src_q + off, 16, 1024), C::kIdescST, kk > 0);
+        }
+      };
+      // acc (+)= A^T-tile from TMEM x B: A = P^T or dS^T packed in X or Y (queries 64w..64w+63
+      // in columns 64w..64w+31), B = dO or Q with the query index as K (MN-major, 16 queries =
+      // 2048 bytes per step)
+      auto acc_mma = [&](uint32_t acc, uint32_t src, uint32_t sb, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          ptx::mma_ts(tmem + acc, tmem + src + (kk / 4) * 64 + (kk % 4) * 8,
+                      ptx::sdesc_sw128(sb + kk * 2048, 128 * 128, 1024), C::kIdescAcc,
+                      (!first || kk > 0) ? 1u : 0u);
+      };
+      bool ok = true;
+      if (total > 0) {
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, lim_ms, a.err);
+        if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full[0]), 0, lim_ms, a.err);
+        if (ok) {
+          ptx::tc_fence_after();
+          st_mma(C::kX, sbase + C::kK, sbase + C::kQ);
+          ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->o_full[0]), 0, lim_ms, a.err);
+        }
+        if (ok) {
+          ptx::tc_fence_after();
+          st_mma(C::kY, sbase + C::kV, sbase + C::kO);
+          ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
+        }
+        for (int n = 0; n < total && ok; ++n) {
+          const int qs = n % C::kQSlots, os = n % C::kOSlots;
+          const int qs1 = (n + 1) % C::kQSlots, os1 = (n + 1) % C::kOSlots;
+          const bool more = n + 1 < total;
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_ready), (uint32_t)n & 1u, lim_ms, a.err);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          acc_mma(C::kDV, C::kX, sbase + C::kO + os * C::kTile, n == 0);
+          ptx::mma_commit(ptx::smem_u32(&bars->o_empty[os]));
+          if (more) {                                 // S^T(n+1) into X, behind dV(n)
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full[qs1]), (uint32_t)((n + 1) / C::kQSlots) & 1u,
+                                lim_ms, a.err);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            st_mma(C::kX, sbase + C::kK, sbase + C::kQ + qs1 * C::kTile);
+            ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+          }
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_ready), (uint32_t)n & 1u, lim_ms, a.err);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          acc_mma(C::kDK, C::kY, sbase + C::kQ + qs * C::kTile, n == 0);
+          ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qs]));
+          if (more) {                                 // dP^T(n+1) into Y, behind dK(n)
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->o_full[os1]), (uint32_t)((n + 1) / C::kOSlots) & 1u,
+                                lim_ms, a.err);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            st_mma(C::kY, sbase + C::kV, sbase + C::kO + os1 * C::kTile);
+            ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
+          }
+        }
+      }
+      ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
+      ptx::mbar_wait(ptx::smem_u32(&bars->acc_done), 0, lim_ms, a.err);
+    }
+  } else {
+    // ------------------------------- compute warpgroups -----------------------------------------
+    const int wg = warp / 4, sub = warp % 4;
+    const int kr = sub * 32 + lane;                  // key row within the tile (TMEM lane)
+    const int key = g.k0 + kr;
+    const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
+    const float c = a.scale * kLog2e;
+    const float2 c2 = make_float2(c, c);
+    const bool key_ok = key < g.kv_lim;
+    const uint32_t tX = tmem + lane_off + C::kX + wg * 64;
+    const uint32_t tY = tmem + lane_off + C::kY + wg * 64;
+    bool ok = true;
+    int n = 0;
+    for (int hg = 0; hg < G && ok; ++hg)
+    for (int i = g.next(g.i_begin); i < g.i_end; i = g.next(i + 1), ++n) {
+      const int vs = n & 1;
+      // the vectors of this tile were written before its Q copy was started
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full[n % C::kQSlots]), (uint32_t)(n / C::kQSlots) & 1u,
+                          lim_ms, a.err);
+      if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full), (uint32_t)n & 1u, lim_ms, a.err);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const float* lse2 = reinterpret_cast<const float*>(smem + C::kVec + vs * 1024) + wg * 64;
+      const float* dl = lse2 + 128;
+      const int kind = g.kind(i);
+      const int q0 = i * BM + wg * 64;               // first query column of this warpgroup
+      // P^T for this thread's key row over 64 query columns
+      float p[64];
+      {
+        uint32_t raw[2][32];
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) ptx::tmem_ld32(tX + hc * 32, raw[hc]);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          ptx::reg_fence(raw[hc]);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {          // column pairs: packed fp32 arithmetic
+            const int col = hc * 32 + e;
+            const float2 nl = *reinterpret_cast<const float2*>(lse2 + col);
+            const float2 x = ptx::fma2(make_float2(__uint_as_float(raw[hc][e]), __uint_as_float(raw[hc][e + 1])),
+                                       c2, nl);
+            float v0 = ptx::ex2(x.x), v1 = ptx::ex2(x.y);
+            if (kind == kPartial) {
+              v0 = (key_ok && (!g.causal || key <= q0 + col)) ? v0 : 0.f;
+              v1 = (key_ok && (!g.causal || key <= q0 + col + 1)) ? v1 : 0.f;
+            }
+            p[col] = v0;
+            p[col + 1] = v1;
+          }
+        }
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
+        ptx::tmem_st32(tX, pk);
+        ptx::tmem_wait_st();
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_ready));
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->dp_full), (uint32_t)n & 1u, lim_ms, a.err);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      // dS^T = P^T * (dP^T - D)
+      {
+        uint32_t raw[2][32];
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) ptx::tmem_ld32(tY + hc * 32, raw[hc]);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          ptx::reg_fence(raw[hc]);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int col = hc * 32 + e;
+            const float2 dd = ptx::sub2(make_float2(__uint_as_float(raw[hc][e]), __uint_as_float(raw[hc][e + 1])),
+                                        *reinterpret_cast<const float2*>(dl + col));
+            const float2 ds = ptx::mul2(make_float2(p[col], p[col + 1]), dd);
+            p[col] = ds.x;
+            p[col + 1] = ds.y;
+          }
+        }
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
+        ptx::tmem_st32(tY, pk);
+        ptx::tmem_wait_st();
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(ptx::smem_u32(&bars->ds_ready));
+        ptx::mbar_arrive(ptx::smem_u32(&bars->vec_empty[vs]));   // this tile's vectors are read
+      }
+    }
+    // ------------------------------- epilogue: dV (warpgroup 0), dK (warpgroup 1) --------------
+    const bool have = ok && n > 0;
+    if (have) {
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_done), 0, lim_ms, a.err);
+      ptx::tc_fence_after();
+    }
+    const float mult = wg == 0 ? 1.f : a.scale;
+    uint16_t* out = static_cast<uint16_t*>(wg == 0 ? a.dv : a.dk) + ((size_t)bh * a.N + key) * D;
+    const uint32_t src = wg == 0 ? C::kDV : C::kDK;
+#pragma unroll 1
+    for (int hc = 0; hc < D / 32; ++hc) {
+      uint32_t raw[32];
+      if (have && ok) {
+        ptx::tmem_ld32(tmem + lane_off + src + hc * 32, raw);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(raw);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) raw[e] = 0u;
+      }
+      if (key < a.N) {
+        uint4* dst = reinterpret_cast<uint4*>(out + hc * 32);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          uint4 w;
+          w.x = ptx::pack2<F16>(__uint_as_float(raw[8 * v4 + 0]) * mult, __uint_as_float(raw[8 * v4 + 1]) * mult);
+          w.y = ptx::pack2<F16>(__uint_as_float(raw[8 * v4 + 2]) * mult, __uint_as_float(raw[8 * v4 + 3]) * mult);
+          w.z = ptx::pack2<F16>(__uint_as_float(raw[8 * v4 + 4]) * mult, __uint_as_float(raw[8 * v4 + 5]) * mult);
+          w.w = ptx::pack2<F16>(__uint_as_float(raw[8 * v4 + 6]) * mult, __uint_as_float(raw[8 * v4 + 7]) * mult);
+          dst[v4] = w;
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 9) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace dkdv
+}  // namespace fa

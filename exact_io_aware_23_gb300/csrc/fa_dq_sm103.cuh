@@ -13,7 +13,9 @@
 // is recomputing S and dP (two more products per tile pair than the fused kernel spends on dQ).
 //
 // GB300 design: one CTA per 128-row query tile of one (b, h) slice, 320 threads.
-//   warp 8      TMA producer: Q_i and dO_i once; K_j, V_j through a ring of stages.
+//   warp 8      TMA producer: Q_i and dO_i once; K_j and V_j through two rings.  V_j is free
+//               once dP has read it, K_j only after dQ has: the K ring is the deeper one, so the
+//               next K tile is loaded a whole tile ahead of the product that needs it.
 //   warp 9      MMA issuer: S = Q_i K_j^T into one of two S buffers (SS); dQ += dS K_{j-1}
 //               for the previous tile (TS: dS read from TMEM, K MN-major in shared memory),
 //               then dP = dO_i V_j^T (SS).  The tensor pipe runs the next tile's S while the
@@ -24,6 +26,8 @@
 //               64 S columns (no other warp reads them).  At the end each warpgroup converts
 //               half of dQ's columns and stores them.
 //   TMEM: dQ [0,128) (d columns used), S buffers [128,256) and [256,384), dP [384,512).
+#pragma once
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -34,7 +38,7 @@
 #include "ptx_sm103.cuh"
 
 namespace fa {
-namespace {
+namespace dqp {
 
 constexpr int BM = 128;          // query rows per CTA
 constexpr int BN = 128;          // keys per tile
@@ -45,21 +49,25 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int D, bool F16>
 struct Cfg {
   static constexpr int kTile = 128 * D * 2;                  // one 128-row operand tile
-  static constexpr int kStages = D == 64 ? 4 : 2;            // K/V ring
+  static constexpr int kKSlots = D == 64 ? 4 : 3;            // K ring
+  static constexpr int kVSlots = D == 64 ? 4 : 2;            // V ring
   static constexpr int kQ = 0;
   static constexpr int kDO = kQ + kTile;
-  static constexpr int kKV = kDO + kTile;                    // stage s: K at kKV + 2s*kTile, V next
-  static constexpr int kBar = kKV + kStages * 2 * kTile;
+  static constexpr int kK = kDO + kTile;                     // K slot s at kK + s*kTile
+  static constexpr int kV = kK + kKSlots * kTile;            // V slot s at kV + s*kTile
+  static constexpr int kBar = kV + kVSlots * kTile;
   static constexpr int kSmem = kBar + 256;
   static constexpr uint32_t kDQ = 0, kS = 128, kDP = 384;    // TMEM columns; S buffer b at kS + 128b
   static constexpr uint32_t kIdescS = ptx::idesc_f32acc(128, 128, false, false, F16);  // S, dP
   static constexpr uint32_t kIdescDQ = ptx::idesc_f32acc(128, D, false, true, F16);    // dQ
 };
 
-struct Bars {             // at most 128 bytes (the live-tile bitmap follows)
+struct Bars {             // at most 256 bytes (the live-tile bitmap follows)
   uint64_t q_full;
-  uint64_t kv_full[4];
-  uint64_t kv_empty[4];
+  uint64_t k_full[4];
+  uint64_t k_empty[4];
+  uint64_t v_full[4];
+  uint64_t v_empty[4];
   uint64_t s_full[2];
   uint64_t dp_full;
   uint64_t ds_ready;
@@ -67,7 +75,7 @@ struct Bars {             // at most 128 bytes (the live-tile bitmap follows)
   uint32_t tmem_base;
 };
 
-static_assert(sizeof(Bars) <= 128, "the live-tile bitmap starts 128 bytes after the barriers");
+static_assert(sizeof(Bars) <= 256, "the live-tile bitmap starts 256 bytes after the barriers");
 
 enum : int { kNone = 0, kPartial = 1, kFull = 2 };
 
@@ -97,10 +105,9 @@ struct Geo {
 };
 
 template <int D, bool F16>
-__global__ void __launch_bounds__(kThreads, 1)
-dq_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                BwdArgs a) {
+__device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                    const CUtensorMap& tmV, const CUtensorMap& tmDO,
+                                    const BwdArgs& a) {
   using C = Cfg<D, F16>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -115,8 +122,8 @@ dq_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   // K/V stream in L2.
   const int BH = a.B * a.H;
   const int n_qt = (a.N + BM - 1) / BM;
-  const int bh = a.heads_fastest ? (int)(blockIdx.x % BH) : (int)(blockIdx.x / n_qt);
-  const int it = a.heads_fastest ? (int)(blockIdx.x / BH) : (int)(blockIdx.x % n_qt);
+  const int bh = a.heads_fastest ? unit % BH : unit / n_qt;
+  const int it = a.heads_fastest ? unit / BH : unit % n_qt;
   const int b = bh / a.H;
   // grouped-query attention: query head h reads key/value head h / (H / Hkv)
   const int bh_kv = b * a.Hkv + (bh % a.H) / (a.H / a.Hkv);
@@ -137,9 +144,13 @@ dq_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars->kv_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[s]), 1);
+    for (int s = 0; s < C::kKSlots; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->k_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->k_empty[s]), 1);
+    }
+    for (int s = 0; s < C::kVSlots; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->v_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->v_empty[s]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&bars->s_full[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->s_full[1]), 1);
@@ -154,7 +165,7 @@ dq_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   }
   g.bits = nullptr;
   if (a.block_mask != nullptr) {                 // live-tile bitmap, one ballot per 32 tiles
-    uint32_t* live_bits = reinterpret_cast<uint32_t*>(smem + C::kBar + 128);
+    uint32_t* live_bits = reinterpret_cast<uint32_t*>(smem + C::kBar + 256);
     g.bits = live_bits;
     for (int w = warp; w < (g.j_end + 31) / 32; w += kThreads / 32) {
       const int j = w * 32 + lane;
@@ -180,34 +191,41 @@ dq_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ptx::tma_load_3d(sbase + C::kDO + hh * 128 * 128, &tmDO, qb, hh * 64, g.q0, bh);
       }
       for (int j = g.next(0); j < g.j_end && ok; j = g.next(j + 1), ++n) {
-        const int stg = n % C::kStages;
-        const uint32_t ph = (uint32_t)(n / C::kStages) & 1u;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[stg]), ph ^ 1u, lim_ms, a.err);
+        const int ks = n % C::kKSlots, vs = n % C::kVSlots;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_empty[ks]), ((uint32_t)(n / C::kKSlots) & 1u) ^ 1u,
+                            lim_ms, a.err);
         if (!ok) break;
-        const uint32_t fb = ptx::smem_u32(&bars->kv_full[stg]);
-        ptx::mbar_arrive_expect_tx(fb, 2 * C::kTile);
-        const uint32_t sk = sbase + C::kKV + stg * 2 * C::kTile;
-        for (int hh = 0; hh < D / 64; ++hh) {
-          ptx::tma_load_3d(sk + hh * 128 * 128, &tmK, fb, hh * 64, j * BN, bh_kv);
-          ptx::tma_load_3d(sk + C::kTile + hh * 128 * 128, &tmV, fb, hh * 64, j * BN, bh_kv);
-        }
+        const uint32_t kb = ptx::smem_u32(&bars->k_full[ks]);
+        ptx::mbar_arrive_expect_tx(kb, C::kTile);
+        for (int hh = 0; hh < D / 64; ++hh)
+          ptx::tma_load_3d(sbase + C::kK + ks * C::kTile + hh * 128 * 128, &tmK, kb, hh * 64, j * BN, bh_kv);
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[vs]), ((uint32_t)(n / C::kVSlots) & 1u) ^ 1u,
+                            lim_ms, a.err);
+        if (!ok) { ++n; break; }
+        const uint32_t vb = ptx::smem_u32(&bars->v_full[vs]);
+        ptx::mbar_arrive_expect_tx(vb, C::kTile);
+        for (int hh = 0; hh < D / 64; ++hh)
+          ptx::tma_load_3d(sbase + C::kV + vs * C::kTile + hh * 128 * 128, &tmV, vb, hh * 64, j * BN, bh_kv);
       }
       // drain: copies in flight must land before shared memory is released
       ptx::mbar_wait(qb, 0, lim_ms, a.err);
-      for (int m = max(0, n - C::kStages); m < n; ++m)
-        ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[m % C::kStages]), (uint32_t)(m / C::kStages) & 1u,
+      for (int m = max(0, n - C::kKSlots); m < n; ++m)
+        ptx::mbar_wait(ptx::smem_u32(&bars->k_full[m % C::kKSlots]), (uint32_t)(m / C::kKSlots) & 1u,
+                       lim_ms, a.err);
+      for (int m = max(0, n - C::kVSlots); m < n; ++m)
+        ptx::mbar_wait(ptx::smem_u32(&bars->v_full[m % C::kVSlots]), (uint32_t)(m / C::kVSlots) & 1u,
                        lim_ms, a.err);
     }
   } else if (warp == 9) {
     // ------------------------------- MMA issuer -------------------------------------------------
     if (lane == 0) {
       bool ok = true;
-      int n = 0, prev_stg = 0;
+      int n = 0;
       // dQ += dS(m) K(m): A = dS packed in S buffer m&1 (keys 64w..64w+63 in its columns
       // 64w..64w+31), B = K_m with the key index as K (MN-major, 16 keys = 2048 bytes a step)
-      auto dq_mma = [&](int m, int stg) {
+      auto dq_mma = [&](int m) {
         const uint32_t sb = C::kS + (uint32_t)(m & 1) * 128;
-        const uint32_t sk = sbase + C::kKV + stg * 2 * C::kTile;
+        const uint32_t sk = sbase + C::kK + (m % C::kKSlots) * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           ptx::mma_ts(tmem + C::kDQ, tmem + sb + (kk / 4) * 64 + (kk % 4) * 8,
@@ -217,12 +235,12 @@ dq_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       if (any) {
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, lim_ms, a.err);
         for (int j = g.next(0); j < g.j_end && ok; j = g.next(j + 1), ++n) {
-          const int stg = n % C::kStages;
-          ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[stg]), (uint32_t)(n / C::kStages) & 1u,
+          const int ks = n % C::kKSlots, vs = n % C::kVSlots;
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_full[ks]), (uint32_t)(n / C::kKSlots) & 1u,
                               lim_ms, a.err);
           if (!ok) break;
           ptx::tc_fence_after();
-          const uint32_t sk = sbase + C::kKV + stg * 2 * C::kTile;
+          const uint32_t sk = sbase + C::kK + ks * C::kTile;
           // S(n) = Q K_j^T (K-major operands, k-steps of 16 along d).  Its buffer last held
           // dS(n-2), read by dQ(n-2), which was issued before this.
           const uint32_t sb = C::kS + (uint32_t)(n & 1) * 128;
@@ -238,25 +256,30 @@ dq_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_ready), (uint32_t)(n - 1) & 1u, lim_ms, a.err);
             if (!ok) break;
             ptx::tc_fence_after();
-            dq_mma(n - 1, prev_stg);
-            ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[prev_stg]));
+            dq_mma(n - 1);
+            ptx::mma_commit(ptx::smem_u32(&bars->k_empty[(n - 1) % C::kKSlots]));
           }
-          // dP(n) = dO V_j^T
+          // dP(n) = dO V_j^T; V_j is free once this product is done
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_full[vs]), (uint32_t)(n / C::kVSlots) & 1u,
+                              lim_ms, a.err);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint32_t sv = sbase + C::kV + vs * C::kTile;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
             ptx::mma_ss(tmem + C::kDP, ptx::sdesc_sw128(sbase + C::kDO + off, 16, 1024),
-                        ptx::sdesc_sw128(sk + C::kTile + off, 16, 1024), C::kIdescS, kk > 0);
+                        ptx::sdesc_sw128(sv + off, 16, 1024), C::kIdescS, kk > 0);
           }
           ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
-          prev_stg = stg;
+          ptx::mma_commit(ptx::smem_u32(&bars->v_empty[vs]));
         }
         if (ok && n > 0) {
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_ready), (uint32_t)(n - 1) & 1u, lim_ms, a.err);
           if (ok) {
             ptx::tc_fence_after();
-            dq_mma(n - 1, prev_stg);
-            ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[prev_stg]));
+            dq_mma(n - 1);
+            ptx::mma_commit(ptx::smem_u32(&bars->k_empty[(n - 1) % C::kKSlots]));
           }
         }
       }
@@ -383,41 +406,5 @@ dq_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (warp == 9) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
-cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH, bool f16) {
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return encode_tensor_map(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                           3, base, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
-template <int D, bool F16>
-cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
-  CUtensorMap mq, mk, mv, mdo;
-  const int BH = a.B * a.H;            // query slices (Q, dO, dQ)
-  const int BHkv = a.B * a.Hkv;        // key/value slices (K, V)
-  cudaError_t e;
-  if ((e = make_map(&mq, a.q, D, a.N, BH, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, a.k, D, a.N, BHkv, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, a.v, D, a.N, BHkv, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mdo, a.dO, D, a.N, BH, F16)) != cudaSuccess) return e;
-  auto kern = dq_sm103_kernel<D, F16>;
-  // barriers (128 bytes) + the live-tile bitmap of a block-sparse mask (one bit per key tile)
-  int smem = Cfg<D, F16>::kSmem;
-  if (a.block_mask != nullptr) smem = max(smem, Cfg<D, F16>::kBar + 128 + ((a.n_tiles + 127) / 128) * 16);
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid(((a.N + BM - 1) / BM) * BH);
-  kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mdo, a);
-  return cudaGetLastError();
-}
-
-}  // namespace
-
-cudaError_t launch_dq_sm103(const BwdArgs& a, fa_dtype dt, cudaStream_t s) {
-  if (dt == FA_FP16) return a.d == 64 ? launch<64, true>(a, s) : launch<128, true>(a, s);
-  return a.d == 64 ? launch<64, false>(a, s) : launch<128, false>(a, s);
-}
-
+}  // namespace dqp
 }  // namespace fa

@@ -12,12 +12,13 @@ namespace fa {
 cudaError_t launch_fwd_sm103(const FwdArgs& a, fa_dtype dt, cudaStream_t s);
 
 // bf16 / fp16 backward main kernel (tcgen05 + TMA), d in {64, 128}; runs between the
-// preprocess and the dQ conversion kernels.  With a.deterministic it computes dK and dV only.
+// preprocess and the dQ conversion kernels.
 cudaError_t launch_bwd_sm103(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
 
-// bf16 / fp16 dQ pass of the deterministic backward (tcgen05 + TMA), d in {64, 128}: one CTA
-// per 128-row query tile, keys visited in a fixed order, dQ written once.
-cudaError_t launch_dq_sm103(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
+// bf16 / fp16 deterministic backward, both tensor-core passes in one launch (tcgen05 + TMA),
+// d in {64, 128}: key-stationary CTAs write dK and dV, query-stationary CTAs write dQ; no result
+// is added from several CTAs.
+cudaError_t launch_bwd_split_sm103(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
 
 // Encodes a tiled TMA descriptor through the driver entry point (resolved once per process).
 cudaError_t encode_tensor_map(CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank,

@@ -39,6 +39,13 @@ What it computes, and where the pages fix it:
   backward, dK and dV of a key/value head are the sums over the query heads that read it (the
   chain rule through the shared operand).
 
+* Ragged offsets and document masks (page 3, same list: "document mask" and "ragged offsets").
+  The pages name them only.  Reading: several sequences (documents) of lengths L_0, L_1, ...
+  are packed back to back along the token axis, described by offsets ``segments`` =
+  [0, L_0, L_0+L_1, ..., total]; a query attends only to keys of its own sequence (the
+  document mask), and with ``causal`` only to keys at or before it.  Packed this way, B = 1 and
+  N = total.
+
 Large inputs are processed a chunk of query rows at a time (a memory bound only: each chunk
 still forms its full score rows).  When a tile mask removes most columns, a chunk gathers
 the columns that any of its rows may attend to; every other column is masked for the whole
@@ -68,10 +75,17 @@ def kv_head(h: int, H: int, Hkv: int) -> int:
     return h // (H // Hkv)
 
 
+def segment_of(x: np.ndarray, segments) -> np.ndarray:
+    """Index of the packed sequence that holds each position (offsets [0, ..., total])."""
+    return np.searchsorted(np.asarray(segments, dtype=np.int64), x, side="right") - 1
+
+
 def allowed(rows: np.ndarray, cols: np.ndarray, causal: bool, kv_len: Optional[int],
-            block_mask: Optional[np.ndarray]) -> np.ndarray:
+            block_mask: Optional[np.ndarray], segments=None) -> np.ndarray:
     """Boolean [len(rows), len(cols)]: which (query, key) pairs enter the softmax."""
     ok = np.ones((rows.size, cols.size), dtype=bool)
+    if segments is not None:
+        ok &= segment_of(rows, segments)[:, None] == segment_of(cols, segments)[None, :]
     if causal:
         ok &= cols[None, :] <= rows[:, None]
     if kv_len is not None:
@@ -82,12 +96,13 @@ def allowed(rows: np.ndarray, cols: np.ndarray, causal: bool, kv_len: Optional[i
     return ok
 
 
-def _chunk_cols(rows: np.ndarray, N: int, causal: bool, kv_len, block_mask) -> np.ndarray:
+def _chunk_cols(rows: np.ndarray, N: int, causal: bool, kv_len, block_mask,
+                segments=None) -> np.ndarray:
     """Columns any row of the chunk may attend to (all N when nothing restricts them)."""
-    if block_mask is None and kv_len is None and not causal:
+    if block_mask is None and kv_len is None and not causal and segments is None:
         return np.arange(N)
     cols = np.arange(N)
-    ok = allowed(rows, cols, causal, kv_len, block_mask)
+    ok = allowed(rows, cols, causal, kv_len, block_mask, segments)
     keep = ok.any(axis=0)
     return cols[keep]
 
@@ -114,21 +129,32 @@ def _probs(s: np.ndarray, lse: np.ndarray) -> np.ndarray:
     return p
 
 
+def _check_segments(segments, B: int, N: int, kv_lens):
+    if segments is None:
+        return
+    seg = np.asarray(segments, dtype=np.int64)
+    if B != 1 or kv_lens is not None or seg[0] != 0 or seg[-1] != N or np.any(np.diff(seg) < 0):
+        raise ValueError("packed sequences need B = 1, no kv_lens and offsets 0 <= ... <= N = total")
+
+
 def forward(q, k, v, scale: float, causal: bool = False, kv_lens=None, block_mask=None,
-            rows: Optional[Sequence[int]] = None, heads: Optional[Sequence[int]] = None):
+            rows: Optional[Sequence[int]] = None, heads: Optional[Sequence[int]] = None,
+            segments=None):
     """Dense masked attention in fp64.
 
     q: float64 array [B, H, N, d]; k, v: [B, Hkv, N, d] with Hkv dividing H (query head h reads
     key/value head h // (H / Hkv); Hkv = H is ordinary multi-head attention).  k and v may have
     a different N only when neither causal nor a block mask is set.  Returns
     (O [B,H,R,d], LSE [B,H,R]) for the R query rows in ``rows`` (default: all rows) and the
-    heads in ``heads`` (default: all heads).
+    heads in ``heads`` (default: all heads).  ``segments``: offsets of packed sequences along
+    the token axis (B = 1); a query sees only the keys of its own sequence.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
+    _check_segments(segments, B, Nq, kv_lens)
     rows = np.arange(Nq) if rows is None else np.asarray(rows, dtype=np.int64)
     heads = list(range(H)) if heads is None else list(heads)
     lens = _as_i64_list(kv_lens, B)
@@ -140,8 +166,8 @@ def forward(q, k, v, scale: float, causal: bool = False, kv_lens=None, block_mas
             g = kv_head(h, H, Hkv)
             for c0 in range(0, rows.size, ROW_CHUNK):
                 r = rows[c0:c0 + ROW_CHUNK]
-                cols = _chunk_cols(r, Nk, causal, lens[b], block_mask)
-                ok = allowed(r, cols, causal, lens[b], block_mask)
+                cols = _chunk_cols(r, Nk, causal, lens[b], block_mask, segments)
+                ok = allowed(r, cols, causal, lens[b], block_mask, segments)
                 s = _scores(q[b, h, r], k[b, g, cols], scale, ok)
                 lse = _row_lse(s)
                 p = _probs(s, lse)
@@ -161,13 +187,13 @@ def probabilities(q, k, scale: float, causal: bool = False, kv_len=None, block_m
 
 def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, block_mask=None,
              heads: Optional[Sequence[int]] = None, return_delta: bool = False,
-             rows: Optional[Sequence[int]] = None, o=None):
+             rows: Optional[Sequence[int]] = None, o=None, segments=None):
     """Explicit-gradient backward of dense masked attention, fp64.
 
     Returns (dQ, dK, dV), each [B, len(heads), N, d]; with ``return_delta`` also D [B,H',N].
     With fewer key/value heads than query heads (k, v [B, Hkv, N, d]; see ``forward``), dK and
     dV are [B, Hkv, N, d] and each key/value head sums the contributions of the selected query
-    heads that read it.
+    heads that read it.  ``segments`` as in ``forward``.
     D_i = sum_j P_ij dP_ij, the exact gradient's row term.  When the forward output ``o``
     ([B,H,N,d]) is given, D_i = sum_c dO_ic o_ic instead: the backward as an operator of its
     inputs (q, k, v, o, dO, LSE), the form the method's backward takes (equal to the first
@@ -180,6 +206,7 @@ def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, bloc
     v = np.asarray(v, dtype=np.float64)
     do = np.asarray(do, dtype=np.float64)
     B, H, N, d = q.shape
+    _check_segments(segments, B, N, kv_lens)
     heads = list(range(H)) if heads is None else list(heads)
     lens = _as_i64_list(kv_lens, B)
     Hkv = k.shape[1]
@@ -195,8 +222,8 @@ def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, bloc
             kvi = g if grouped else hi
             for c0 in range(0, all_rows.size, ROW_CHUNK):
                 r = all_rows[c0:c0 + ROW_CHUNK]
-                cols = _chunk_cols(r, k.shape[2], causal, lens[b], block_mask)
-                ok = allowed(r, cols, causal, lens[b], block_mask)
+                cols = _chunk_cols(r, k.shape[2], causal, lens[b], block_mask, segments)
+                ok = allowed(r, cols, causal, lens[b], block_mask, segments)
                 s = _scores(q[b, h, r], k[b, g, cols], scale, ok)
                 p = _probs(s, _row_lse(s))
                 dp = do[b, h, r] @ v[b, g, cols].T

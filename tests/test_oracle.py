@@ -383,6 +383,57 @@ def test_gqa_head_mapping_rejects_non_divisors():
         oa.kv_head(0, 6, 4)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_sequences_equal_separate_calls(causal):
+    """Sequences packed along the token axis with offsets (the document mask) give, row for row,
+    what attention on each sequence alone gives; dK, dV likewise (a key is seen only by its own
+    sequence's queries).  Includes an empty sequence and lengths off the 128 grid."""
+    lens = [5, 0, 130, 1, 64]
+    seg = np.concatenate([[0], np.cumsum(lens)])
+    T, H, d = int(seg[-1]), 2, 4
+    q, k, v, do = (_rand((1, H, T, d), s) for s in (170, 171, 172, 173))
+    O, L = oracle.forward(q, k, v, 0.45, causal=causal, segments=seg)
+    dQ, dK, dV = oracle.backward(q, k, v, do, 0.45, causal=causal, segments=seg)
+    for a, b in zip(seg[:-1], seg[1:]):
+        if a == b:
+            continue
+        sl = slice(int(a), int(b))
+        O1, L1 = oracle.forward(q[:, :, sl], k[:, :, sl], v[:, :, sl], 0.45, causal=causal)
+        g1 = oracle.backward(q[:, :, sl], k[:, :, sl], v[:, :, sl], do[:, :, sl], 0.45, causal=causal)
+        assert np.max(np.abs(O[:, :, sl] - O1)) < 1e-13 and np.max(np.abs(L[:, :, sl] - L1)) < 1e-13
+        for full, part in zip((dQ, dK, dV), g1):
+            assert np.max(np.abs(full[:, :, sl] - part)) < 1e-12
+
+
+def test_packed_sequence_starts_see_only_themselves():
+    """Causal and packed: the first token of each sequence attends to itself alone, so its
+    output is its own value row and its LSE is its own scaled score."""
+    seg = np.array([0, 3, 4, 9])
+    q, k, v = (_rand((1, 1, 9, 3), s) for s in (180, 181, 182))
+    O, L = oracle.forward(q, k, v, 0.9, causal=True, segments=seg)
+    for a in seg[:-1]:
+        assert np.max(np.abs(O[0, 0, a] - v[0, 0, a])) < 1e-14
+        assert abs(L[0, 0, a] - 0.9 * float(q[0, 0, a] @ k[0, 0, a])) < 1e-13
+
+
+def test_packed_sequences_finite_differences():
+    seg = np.array([0, 4, 9])
+    q, k, v, do = (_rand((1, 1, 9, 2), s, 1.1) for s in (190, 191, 192, 193))
+    dQ, dK, dV = oracle.backward(q, k, v, do, 0.6, causal=True, segments=seg)
+    h = 1e-6
+    for name, x, g in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+        for f in range(x.size):
+            idx = tuple(int(i) for i in np.unravel_index(f, x.shape))
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args = {"q": q, "k": k, "v": v}
+            lp = _loss(**{**args, name: xp}, do=do, scale=0.6, causal=True, segments=seg)
+            lm = _loss(**{**args, name: xm}, do=do, scale=0.6, causal=True, segments=seg)
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(g[idx])), (name, idx, fd, g[idx])
+
+
 def test_backward_delta_both_ways_and_sums():
     """D_i = sum_j P_ij dP_ij equals rowsum(dO * O); sum_j dK_j = 0; sum_j dV_j = sum_i dO_i."""
     B, H, N, d = 1, 2, 200, 8

@@ -1,8 +1,8 @@
 """Plant plausible mistakes in a copy of the oracle (on the CPU) and check that the pins in
 test_oracle.py catch every one: a dropped scale, a sign, a transposed operand, an off-by-one in
 each mask, the wrong logarithm base, a wrong reduction axis, a wrong rescale direction in the
-pages' online algorithm, a wrong factor in the pages' merge law and a wrong query-to-key/value
-head mapping."""
+pages' online algorithm, a wrong factor in the pages' merge law a wrong query-to-key/value
+head mapping and a sequence boundary off by one."""
 import os
 import shutil
 import subprocess
@@ -32,6 +32,8 @@ MUTATIONS = [
      "return m, fa * la + fb * lb, fa * np.asarray(ua) + fa * np.asarray(ub)"),
     ("return h // (H // Hkv)", "return h % Hkv"),
     ("kvi = g if grouped else hi", "kvi = hi % Hkv if grouped else hi"),
+    ('return np.searchsorted(np.asarray(segments, dtype=np.int64), x, side="right") - 1',
+     'return np.searchsorted(np.asarray(segments, dtype=np.int64), x, side="left") - 1'),
 ]
 
 
