@@ -201,6 +201,8 @@ def run_ours(args, w):
         if world > 1:
             dist.barrier()
 
+    if args.fused_backward:
+        fa.set_backward_variant(fa.BWD_FUSED_ATOMIC)
     x = make_inputs(w, seed=rank)
     B, H, N, d = x["q"].shape
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
@@ -296,7 +298,7 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": dict(workload_config(w),
-                       **({"deterministic_backward": True} if args.deterministic else {})),
+                       backward="fused_atomic_dq" if args.fused_backward else "two_pass"),
         "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
         "fwd_bwd_tflops_algorithmic": world * 3.5 * F / (ms_step * 1e-3) / 1e12,
         "pct_of_bf16_peak": {"forward": fwd_tf / peak, "fwd_bwd": value / world / peak,
@@ -308,7 +310,7 @@ def run_ours(args, w):
                      "peak_source": f"bf16_tflops of {peak_src}"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP["fused" if args.fused_backward else "two_pass"] * args.steps,
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -325,9 +327,9 @@ def run_ours(args, w):
         print(json.dumps(line), flush=True)
 
 
-# kernels of ours launched per step: forward 1, backward 3 (preprocess, main, dQ convert; with
-# --deterministic: preprocess, dK/dV kernel, dQ kernel)
-LAUNCHES_PER_STEP = 4
+# kernels of ours launched per step: forward 1; backward 2 (preprocess, two-pass kernel) or, with
+# --fused-backward, 3 (preprocess, fused kernel, dQ convert)
+LAUNCHES_PER_STEP = {"two_pass": 3, "fused": 4}
 
 
 def run_decode(args, w):
@@ -411,7 +413,9 @@ def main():
     ap.add_argument("--workload", default="long_n16k_d128")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--deterministic", action="store_true",
-                    help="time the bit-reproducible backward (fa_backward_deterministic)")
+                    help="call fa_backward_deterministic (the default two-pass backward, by name)")
+    ap.add_argument("--fused-backward", action="store_true",
+                    help="time the fused atomic-dQ backward variant (fa_set_backward_variant)")
     ap.add_argument("--cpu-rows", type=int, default=16384)
     ap.add_argument("--ref-rows", type=int, default=1024)
     args = ap.parse_args()

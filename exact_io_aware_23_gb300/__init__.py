@@ -62,6 +62,8 @@ def _load() -> ctypes.CDLL:
     L.fa_backward_deterministic.restype = i
     L.fa_backward_deterministic_workspace_size.argtypes = [i, i, i]
     L.fa_backward_deterministic_workspace_size.restype = sz
+    L.fa_set_backward_variant.argtypes = [i]
+    L.fa_set_backward_variant.restype = i
     L.fa_forward_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, i, vp, sz, vp]
     L.fa_forward_splitkv.restype = i
     L.fa_forward_splitkv_workspace_size.argtypes = [i, i, i, i, i]
@@ -233,6 +235,16 @@ def set_fault_injection(mode: int) -> None:
 
 def set_wait_limit_ms(ms: int) -> None:
     lib.fa_debug_set_wait_limit_ms(int(ms))
+
+
+BWD_TWO_PASS, BWD_FUSED_ATOMIC = 0, 1
+
+
+def set_backward_variant(variant: int) -> None:
+    """fa_set_backward_variant: BWD_TWO_PASS (default, deterministic) or BWD_FUSED_ATOMIC."""
+    st = lib.fa_set_backward_variant(int(variant))
+    if st != FA_OK:
+        raise FaError(st, "fa_set_backward_variant")
 
 
 def backward_noalloc(q, k, v, o, lse, do, *, causal: bool = False, scale: Optional[float] = None,

@@ -18,6 +18,7 @@ constexpr int kMaxDevices = 64;
 int* g_err_ptr[kMaxDevices] = {nullptr};
 std::atomic<int> g_inject{0};
 std::atomic<uint32_t> g_wait_limit_ms{2000};
+std::atomic<int> g_bwd_variant{FA_BWD_TWO_PASS};
 
 fa_status device_error_word(int** out) {
   int dev = 0;
@@ -86,6 +87,12 @@ const char* fa_status_string(fa_status s) {
 void fa_debug_set_fault_injection(int mode) { g_inject.store(mode); }
 
 void fa_debug_set_wait_limit_ms(uint32_t ms) { g_wait_limit_ms.store(ms == 0 ? 2000u : ms); }
+
+fa_status fa_set_backward_variant(fa_bwd_variant v) {
+  if (v != FA_BWD_TWO_PASS && v != FA_BWD_FUSED_ATOMIC) return FA_ERR_INVALID_ARG;
+  g_bwd_variant.store(v);
+  return FA_OK;
+}
 
 }  // extern "C"
 
@@ -224,6 +231,9 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
   st = check_heads(H, Hkv, dtype);
   if (st != FA_OK) return st;
   if (deterministic && dtype == FA_FP32) return FA_ERR_UNSUPPORTED;
+  // 16-bit inputs run the two-pass backward unless the fused one was selected; fp32 always runs
+  // the CUDA-core backward (which adds dQ from several blocks).
+  const bool two_pass = deterministic || (dtype != FA_FP32 && g_bwd_variant.load() == FA_BWD_TWO_PASS);
   if (B == 0 || H == 0 || N == 0) return FA_OK;
   if (block_mask != nullptr && N > kMaxBlockSparseN) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace)
@@ -238,7 +248,7 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
   fa::BwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.o = o; a.dO = dO; a.lse = lse; a.dq = dq; a.dk = dk; a.dv = dv;
   const size_t rows = (size_t)B * H * N;
-  if (deterministic) {
+  if (two_pass) {                      // D only: dQ is written once, no accumulator
     a.dq_acc = nullptr;
     a.delta = static_cast<float*>(workspace);
   } else {
@@ -246,7 +256,6 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
     a.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                        round_up(rows * (size_t)d * sizeof(float), 256));
   }
-  a.deterministic = deterministic ? 1 : 0;
   a.B = B; a.H = H; a.Hkv = Hkv; a.N = N; a.d = d; a.scale = scale; a.causal = causal != 0;
   a.block_mask = block_mask; a.n_tiles = (N + fa::kMaskTile - 1) / fa::kMaskTile;
   a.kv_lens = kv_lens; a.dbg = knobs();
@@ -257,7 +266,7 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = fa::launch_bwd_preprocess(a, dtype, s);
   if (e == cudaSuccess) {
-    if (deterministic) {
+    if (two_pass) {
       e = fa::launch_bwd_split_sm103(a, dtype, s);
     } else {
       e = dtype == FA_FP32 ? fa::launch_bwd_simt(a, dtype, s) : fa::launch_bwd_sm103(a, dtype, s);

@@ -65,7 +65,7 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  float* dq_acc;    // workspace: fp32 [B, H, N, d]; null in the deterministic backward
+  float* dq_acc;    // workspace: fp32 [B, H, N, d]; null in the two-pass backward
   float* delta;     // workspace: fp32 [B, H, N], D_i = rowsum(dO_i * O_i)
   int B, H, N, d;
   int Hkv;          // key/value heads (K, V, dK, dV are [B, Hkv, N, d])
@@ -77,9 +77,6 @@ struct BwdArgs {
   int* err;
   DebugKnobs dbg;
   int heads_fastest;          // launch order: (b, h) slice fastest (unequal work per tile)
-  // Deterministic backward: the key-stationary kernel produces dK and dV only, and a separate
-  // query-stationary kernel produces dQ with no cross-CTA accumulation.
-  int deterministic;
 };
 
 // CUDA-core (SIMT) kernels: the fp32 path.

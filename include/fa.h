@@ -160,9 +160,10 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d);
  *   workspace   : device scratch of at least fa_backward_workspace_size(B,H,N,d) bytes,
  *                 256-byte aligned, owned by the caller; its contents on entry do not matter
  *                 and are overwritten.  Two calls in flight at once need two workspaces.
- * Other arguments as in fa_forward.  The result of concurrent dQ accumulation is
- * nondeterministic in the last bits (the order of the fp32 additions into the dQ accumulator
- * varies); fa_backward_deterministic is the reproducible variant.
+ * Other arguments as in fa_forward.  bf16 and fp16 run the two-pass backward of
+ * fa_backward_deterministic (dK/dV over key tiles, dQ over query tiles, no cross-block sums):
+ * the same bits on every run.  fp32, and the fused variant that fa_set_backward_variant can
+ * select, add dQ from several blocks in an order that varies in the last bits.
  */
 fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
                       const void* dO, const float* lse, void* dq, void* dk, void* dv,
@@ -211,6 +212,19 @@ const char* fa_status_string(fa_status s);
  */
 void fa_debug_set_fault_injection(int mode);
 void fa_debug_set_wait_limit_ms(uint32_t wait_limit_ms);
+
+/*
+ * Backward variant for bf16/fp16 inputs of fa_backward, fa_backward_gqa and
+ * fa_backward_noalloc (process-wide; fp32 is unaffected):
+ *   FA_BWD_TWO_PASS      (default) the two passes of fa_backward_deterministic in one launch;
+ *   FA_BWD_FUSED_ATOMIC  one key-stationary kernel computing dK, dV and dQ, dQ added into an fp32
+ *                        workspace by the TMA unit from every key tile (fewer matrix products,
+ *                        nondeterministic last bits; slower on most shapes on GB300).
+ * Returns FA_ERR_INVALID_ARG for any other value.  No counterpart in the pages: they describe
+ * one backward and leave its work partition open.
+ */
+typedef enum { FA_BWD_TWO_PASS = 0, FA_BWD_FUSED_ATOMIC = 1 } fa_bwd_variant;
+fa_status fa_set_backward_variant(fa_bwd_variant variant);
 
 /* ABI version of this header: major * 100 + minor. */
 int fa_version(void);

@@ -171,3 +171,11 @@ def test_deterministic_backward_argument_checks(lib):
     assert call(w=ctypes.c_void_p(0x10010)) == INVALID
     assert call(wsb=ws - 4) == INVALID
     assert call(N=0) == OK
+
+
+def test_backward_variant_selector(lib):
+    lib.fa_set_backward_variant.argtypes = [ctypes.c_int]
+    assert lib.fa_set_backward_variant(2) == INVALID
+    assert lib.fa_set_backward_variant(-1) == INVALID
+    assert lib.fa_set_backward_variant(1) == OK
+    assert lib.fa_set_backward_variant(0) == OK           # back to the default

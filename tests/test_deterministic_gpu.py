@@ -1,7 +1,9 @@
-"""GPU parity and reproducibility of the deterministic backward (fa_backward_deterministic): the
-gradients against the fp64 oracle on ragged sizes, every mask, bf16 and fp16, grouped heads;
-the same bits on repeated calls; dK and dV bit-identical to the fused backward's (the same
-key-stationary arithmetic) and dQ within the tolerance of it."""
+"""GPU parity and reproducibility of the two-pass backward (fa_backward_deterministic, and
+fa_backward's default for 16-bit inputs): the gradients against the fp64 oracle on ragged
+sizes, every mask, bf16 and fp16, grouped heads; the same bits on repeated calls and through
+both entry points; dK and dV bit-identical to the fused atomic-dQ backward's (the same
+key-stationary arithmetic) and dQ within the tolerance of it.  The fused variant keeps its own
+parity cases here."""
 import math
 
 import numpy as np
@@ -45,12 +47,28 @@ def test_deterministic_grouped_heads(Hkv):
     compare(x, run_gpu(x, deterministic=True))
 
 
+class _FusedVariant:
+    """Selects the fused atomic-dQ backward for the block (process-wide), then restores."""
+
+    def __enter__(self):
+        import exact_io_aware_23_gb300 as fa
+        fa.set_backward_variant(fa.BWD_FUSED_ATOMIC)
+
+    def __exit__(self, *exc):
+        import exact_io_aware_23_gb300 as fa
+        fa.set_backward_variant(fa.BWD_TWO_PASS)
+
+
 def _both(x, reps=3):
     import exact_io_aware_23_gb300 as fa
     q, k, v, do, kw = _dev(x)
     o, lse = fa.forward(q, k, v, **kw)
     det = [fa.backward(q, k, v, o, lse, do, deterministic=True, **kw) for _ in range(reps)]
-    fused = fa.backward(q, k, v, o, lse, do, **kw)
+    default = fa.backward(q, k, v, o, lse, do, **kw)
+    for a_, b_ in zip(det[0], default):
+        assert torch.equal(a_, b_)
+    with _FusedVariant():
+        fused = fa.backward(q, k, v, o, lse, do, **kw)
     assert fa.check_device_status() == 0
     return det, fused
 
@@ -82,3 +100,29 @@ def test_long_causal_n16k_d128():
     qq, kk, vv, dd = (f64(x[n]) for n in ("q", "k", "v", "do"))
     dQ, _, _ = oracle.backward(qq, kk, vv, dd, x["scale"], causal=True, heads=heads, rows=rows)
     assert_bf16_close("dQ", f64(det[0][0])[:, heads][:, :, rows], dQ[:, :, rows])
+
+
+# --- the fused atomic-dQ variant (fa_set_backward_variant) ----------------------------------
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N,causal", [(300, True), (1000, False)])
+def test_fused_variant_shapes(N, d, causal):
+    x = _case(N, d, causal=causal, seed=7 * N + d)
+    with _FusedVariant():
+        compare(x, run_gpu(x))
+        check_backward_given_o(x)
+
+
+def test_fused_variant_masks_grouped_fp16():
+    x = _case(900, 128, "fp16", True, B=2, H=4, Hkv=2, seed=12)
+    x["kv_lens"] = torch.tensor([900, 451], dtype=torch.int32)
+    x["block_mask"] = random_tile_mask(8, 0.6, seed=5)
+    with _FusedVariant():
+        run_gpu(x, backward=False)
+        check_backward_given_o(x)
+
+
+def test_backward_variant_rejects_unknown():
+    import exact_io_aware_23_gb300 as fa
+    with pytest.raises(fa.FaError):
+        fa.set_backward_variant(7)
