@@ -62,6 +62,11 @@ def _load() -> ctypes.CDLL:
     L.fa_backward_deterministic.restype = i
     L.fa_backward_deterministic_workspace_size.argtypes = [i, i, i]
     L.fa_backward_deterministic_workspace_size.restype = sz
+    L.fa_forward_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
+    L.fa_forward_varlen.restype = i
+    L.fa_backward_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
+                                     i, i, vp, sz, vp]
+    L.fa_backward_varlen.restype = i
     L.fa_set_backward_variant.argtypes = [i]
     L.fa_set_backward_variant.restype = i
     L.fa_forward_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, i, vp, sz, vp]
@@ -144,6 +149,61 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool =
     if st != FA_OK:
         raise FaError(st, "fa_forward")
     return o, lse
+
+
+def _check_packed(q, k, v, cu_seqlens):
+    """q: [H, total, d]; k, v: [Hkv, total, d]; cu_seqlens: int32 [n_seqs + 1] on q's device."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor [heads, total, d]")
+    H, T, d = q.shape
+    Hkv = k.shape[0]
+    if k.shape != v.shape or k.shape[1:] != q.shape[1:] or H % Hkv != 0:
+        raise ValueError("k, v must be [Hkv, total, d] with Hkv dividing the query heads")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DTYPES:
+        raise ValueError("q, k, v must share a supported dtype")
+    if (cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1
+            or cu_seqlens.device != q.device or not cu_seqlens.is_contiguous()):
+        raise ValueError("cu_seqlens must be a contiguous int32 [n_seqs + 1] tensor on q's device")
+    return H, Hkv, T, d, cu_seqlens.numel() - 1
+
+
+def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, causal: bool = False,
+                   scale: Optional[float] = None, stream=None):
+    """fa_forward_varlen: sequences packed along the token axis (q [H, total, d], k, v
+    [Hkv, total, d], offsets cu_seqlens); returns O [H, total, d] and LSE [H, total]."""
+    H, Hkv, T, d, S = _check_packed(q, k, v, cu_seqlens)
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    st = lib.fa_forward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), S,
+                               int(max_seqlen), T, H, Hkv, d, scale, int(bool(causal)),
+                               _DTYPES[q.dtype], _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_forward_varlen")
+    return o, lse
+
+
+def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen: int, *, causal: bool = False,
+                    scale: Optional[float] = None, stream=None):
+    """fa_backward_varlen: dQ [H, total, d], dK, dV [Hkv, total, d] for packed sequences."""
+    H, Hkv, T, d, S = _check_packed(q, k, v, cu_seqlens)
+    for name, t in (("o", o), ("do", do)):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must match q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, T):
+        raise ValueError("lse must be fp32 [H, total]")
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = backward_deterministic_workspace_size(1, H, T)
+    workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib.fa_backward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                                _ptr(dk), _ptr(dv), _ptr(cu_seqlens), S, int(max_seqlen), T, H,
+                                Hkv, d, scale, int(bool(causal)), _DTYPES[q.dtype],
+                                _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_backward_varlen")
+    return dq, dk, dv
 
 
 def forward_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *,

@@ -98,15 +98,22 @@ fa_status fa_set_backward_variant(fa_bwd_variant v) {
 
 namespace {
 
+// Packed sequences (cu_seqlens != null): B sequences, N the longest, `total` tokens per head.
+struct Packing {
+  const int32_t* cu_seqlens;
+  int total;
+};
+
 fa_status forward_impl(const void* q, const void* k, const void* v, void* o, float* lse,
                        int B, int H, int Hkv, int N, int d, float scale, int causal,
                        const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
-                       void* stream) {
+                       void* stream, Packing pk = {nullptr, 0}) {
   fa_status st = check_common(B, H, N, d, scale, dtype);
   if (st != FA_OK) return st;
   st = check_heads(H, Hkv, dtype);
   if (st != FA_OK) return st;
-  if (B == 0 || H == 0 || N == 0) return FA_OK;
+  if (pk.cu_seqlens != nullptr && dtype == FA_FP32) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || N == 0 || (pk.cu_seqlens != nullptr && pk.total == 0)) return FA_OK;
   if (block_mask != nullptr && N > kMaxBlockSparseN) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -120,6 +127,9 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
   // them, the tiles of one slice run together so its K/V (or Q/dO) stream is shared in L2.
   a.heads_fastest = (a.causal || block_mask != nullptr || kv_lens != nullptr) ? 1 : 0;
   a.Nk = N; a.n_splits = 1; a.tiles_per_split = 0; a.o_part = nullptr; a.lse_part = nullptr;
+  a.cu_seqlens = pk.cu_seqlens;
+  a.rows = pk.cu_seqlens != nullptr ? pk.total : N;
+  if (pk.cu_seqlens != nullptr) a.heads_fastest = 1;     // sequences of unequal length
   if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = dtype == FA_FP32 ? fa::launch_fwd_simt(a, dtype, s) : fa::launch_fwd_sm103(a, dtype, s);
@@ -189,6 +199,7 @@ fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* 
   a.block_mask = nullptr; a.n_tiles = (Nq + fa::kMaskTile - 1) / fa::kMaskTile;
   a.kv_lens = kv_lens; a.dbg = knobs(); a.heads_fastest = kv_lens != nullptr ? 1 : 0;
   a.Nk = Nk; a.n_splits = n_splits; a.tiles_per_split = (kv_tiles + n_splits - 1) / n_splits;
+  a.cu_seqlens = nullptr; a.rows = Nq;
   const size_t rows = (size_t)B * H * Nq;
   a.o_part = static_cast<float*>(workspace);
   a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
@@ -225,16 +236,20 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
                         int B, int H, int Hkv, int N, int d, float scale, int causal,
                         const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
                         void* workspace, size_t workspace_bytes, void* stream,
-                        bool deterministic) {
+                        bool deterministic, Packing pk = {nullptr, 0}) {
   fa_status st = check_common(B, H, N, d, scale, dtype);
   if (st != FA_OK) return st;
   st = check_heads(H, Hkv, dtype);
   if (st != FA_OK) return st;
-  if (deterministic && dtype == FA_FP32) return FA_ERR_UNSUPPORTED;
-  // 16-bit inputs run the two-pass backward unless the fused one was selected; fp32 always runs
-  // the CUDA-core backward (which adds dQ from several blocks).
-  const bool two_pass = deterministic || (dtype != FA_FP32 && g_bwd_variant.load() == FA_BWD_TWO_PASS);
-  if (B == 0 || H == 0 || N == 0) return FA_OK;
+  if ((deterministic || pk.cu_seqlens != nullptr) && dtype == FA_FP32) return FA_ERR_UNSUPPORTED;
+  // 16-bit inputs run the two-pass backward unless the fused one was selected (packed sequences
+  // always take the two-pass one); fp32 always runs the CUDA-core backward (which adds dQ from
+  // several blocks).
+  const bool two_pass = deterministic || pk.cu_seqlens != nullptr ||
+                        (dtype != FA_FP32 && g_bwd_variant.load() == FA_BWD_TWO_PASS);
+  // workspace sizes count the query rows of all slices: B*H*N, or H*total when packed
+  const int wB = pk.cu_seqlens != nullptr ? 1 : B, wN = pk.cu_seqlens != nullptr ? pk.total : N;
+  if (B == 0 || H == 0 || N == 0 || (pk.cu_seqlens != nullptr && pk.total == 0)) return FA_OK;
   if (block_mask != nullptr && N > kMaxBlockSparseN) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace)
     return FA_ERR_INVALID_ARG;
@@ -242,12 +257,12 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
       !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
-  const size_t need = deterministic ? fa_backward_deterministic_workspace_size(B, H, N)
-                                    : fa_backward_workspace_size(B, H, N, d);
+  const size_t need = deterministic ? fa_backward_deterministic_workspace_size(wB, H, wN)
+                                    : fa_backward_workspace_size(wB, H, wN, d);
   if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.o = o; a.dO = dO; a.lse = lse; a.dq = dq; a.dk = dk; a.dv = dv;
-  const size_t rows = (size_t)B * H * N;
+  const size_t rows = (size_t)wB * H * wN;
   if (two_pass) {                      // D only: dQ is written once, no accumulator
     a.dq_acc = nullptr;
     a.delta = static_cast<float*>(workspace);
@@ -262,6 +277,9 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
   // Masks make the work per tile unequal: then every slice's heaviest tiles go first.  Without
   // them, the tiles of one slice run together so its K/V (or Q/dO) stream is shared in L2.
   a.heads_fastest = (a.causal || block_mask != nullptr || kv_lens != nullptr) ? 1 : 0;
+  a.cu_seqlens = pk.cu_seqlens;
+  a.rows = pk.cu_seqlens != nullptr ? pk.total : N;
+  if (pk.cu_seqlens != nullptr) a.heads_fastest = 1;     // sequences of unequal length
   if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = fa::launch_bwd_preprocess(a, dtype, s);
@@ -308,6 +326,28 @@ fa_status fa_backward_deterministic(const void* q, const void* k, const void* v,
                        dtype, kv_lens, workspace, workspace_bytes, stream, true);
 }
 
+fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int32_t* cu_seqlens, int n_seqs, int max_seqlen, int total,
+                            int H, int Hkv, int d, float scale, int causal, fa_dtype dtype,
+                            void* stream) {
+  if (n_seqs < 0 || max_seqlen < 0 || total < 0) return FA_ERR_INVALID_ARG;
+  if (n_seqs > 0 && total > 0 && cu_seqlens == nullptr) return FA_ERR_INVALID_ARG;
+  return forward_impl(q, k, v, o, lse, n_seqs, H, Hkv, max_seqlen, d, scale, causal, nullptr,
+                      dtype, nullptr, stream, Packing{cu_seqlens, total});
+}
+
+fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const void* o,
+                             const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                             const int32_t* cu_seqlens, int n_seqs, int max_seqlen, int total,
+                             int H, int Hkv, int d, float scale, int causal, fa_dtype dtype,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_seqs < 0 || max_seqlen < 0 || total < 0) return FA_ERR_INVALID_ARG;
+  if (n_seqs > 0 && total > 0 && cu_seqlens == nullptr) return FA_ERR_INVALID_ARG;
+  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, n_seqs, H, Hkv, max_seqlen, d, scale,
+                       causal, nullptr, dtype, nullptr, workspace, workspace_bytes, stream, true,
+                       Packing{cu_seqlens, total});
+}
+
 fa_status fa_check_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
@@ -318,7 +358,7 @@ fa_status fa_check_device_status(void* stream) {
   if (word != 0) {
     const int zero = 0;
     if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
-    return FA_ERR_TIMEOUT;
+    return word == fa::kDevBadOffsets ? FA_ERR_INVALID_ARG : FA_ERR_TIMEOUT;
   }
   return FA_OK;
 }

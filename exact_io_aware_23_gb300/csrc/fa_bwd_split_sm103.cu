@@ -43,13 +43,16 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH, boo
 template <int D, bool F16>
 cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv, mdo;
-  const int BH = a.B * a.H;            // query slices (Q, dO, dQ)
-  const int BHkv = a.B * a.Hkv;        // key/value slices (K, V, dK, dV)
+  const int BH = a.B * a.H;            // query-side work units per tile row (Q, dO, dQ)
+  const int BHkv = a.B * a.Hkv;        // key/value-side work units per tile row (K, V, dK, dV)
+  // token axis and slice count of the tensor maps: per (b, h) slice, or packed per head
+  const bool packed = a.cu_seqlens != nullptr;
+  const int q_slices = packed ? a.H : BH, kv_slices = packed ? a.Hkv : BHkv;
   cudaError_t e;
-  if ((e = make_map(&mq, a.q, D, a.N, BH, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, a.k, D, a.N, BHkv, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, a.v, D, a.N, BHkv, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mdo, a.dO, D, a.N, BH, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mq, a.q, D, a.rows, q_slices, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, a.k, D, a.rows, kv_slices, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.v, D, a.rows, kv_slices, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mdo, a.dO, D, a.rows, q_slices, F16)) != cudaSuccess) return e;
   auto kern = bwd_split_sm103_kernel<D, F16>;
   // each pass keeps its barriers 256 bytes below its live-tile bitmap (one bit per tile)
   const int bitmap = a.block_mask != nullptr ? ((a.n_tiles + 127) / 128) * 16 : 0;

@@ -126,22 +126,33 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
   const int n_kt = (a.N + BN - 1) / BN;
   const int bh = a.heads_fastest ? unit % BH : unit / n_kt;   // K/V slice
   const int jt = a.heads_fastest ? unit / BH : unit % n_kt;   // key tile
-  const int b = bh / a.Hkv;
+  const int b = bh / a.Hkv, hk = bh % a.Hkv;
   const int G = a.H / a.Hkv;
-  const int bhq0 = b * a.H + (bh % a.Hkv) * G;   // first query slice of the group
+  int row0 = 0, len = a.N;                       // this slice's rows on the token axis
+  if (a.cu_seqlens != nullptr) {
+    // Packed sequences: the grid is sized for the longest one; key tiles past this sequence's
+    // end have nothing to do, and offsets outside the contract are reported, not followed.
+    if (!packed_sequence(a.cu_seqlens, b, a.N, a.rows, &row0, &len)) {
+      if (threadIdx.x == 0) atomicExch(a.err, kDevBadOffsets);
+      return;
+    }
+    if (jt * BN >= len) return;
+  }
+  const int ks = a.cu_seqlens != nullptr ? hk : bh;                            // K, V, dK, dV slice
+  const int bhq0 = (a.cu_seqlens != nullptr ? 0 : b * a.H) + hk * G;            // first query slice
   const uint32_t lim_ms = a.dbg.wait_limit_ms;
 
   Geo g;
   g.k0 = jt * BN;
-  g.N = a.N;
-  int kvl = a.N;
+  g.N = len;
+  int kvl = len;
   if (a.kv_lens != nullptr) kvl = max(0, min(a.N, (int)a.kv_lens[b]));
   g.kv_lim = kvl;
   g.causal = a.causal;
   g.T = a.n_tiles;
   g.bm = a.block_mask;
   g.i_begin = a.causal ? jt : 0;
-  g.i_end = g.k0 < g.kv_lim ? (a.N + BM - 1) / BM : 0;
+  g.i_end = g.k0 < g.kv_lim ? (len + BM - 1) / BM : 0;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bars->kv_full), 1);
@@ -193,8 +204,8 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
         const uint32_t kb = ptx::smem_u32(&bars->kv_full);
         ptx::mbar_arrive_expect_tx(kb, 2 * C::kTile);
         for (int hh = 0; hh < D / 64; ++hh) {
-          ptx::tma_load_3d(sbase + C::kK + hh * 128 * 128, &tmK, kb, hh * 64, g.k0, bh);
-          ptx::tma_load_3d(sbase + C::kV + hh * 128 * 128, &tmV, kb, hh * 64, g.k0, bh);
+          ptx::tma_load_3d(sbase + C::kK + hh * 128 * 128, &tmK, kb, hh * 64, row0 + g.k0, ks);
+          ptx::tma_load_3d(sbase + C::kV + hh * 128 * 128, &tmV, kb, hh * 64, row0 + g.k0, ks);
         }
       }
       for (int hg = 0; hg < G && ok; ++hg)
@@ -214,23 +225,24 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
         float* dl = lse2 + 128;
         for (int r = lane; r < 128; r += 32) {
           const int q = i * BM + r;
-          const float L = q < a.N ? a.lse[(size_t)bhq * a.N + q] : -INFINITY;
+          const size_t row = (size_t)bhq * a.rows + row0 + q;
+          const float L = q < g.N ? a.lse[row] : -INFINITY;
           lse2[r] = L == -INFINITY ? -INFINITY : -L * kLog2e;
-          dl[r] = q < a.N ? a.delta[(size_t)bhq * a.N + q] : 0.f;
+          dl[r] = q < g.N ? a.delta[row] : 0.f;
         }
         __syncwarp();
         if (lane == 0) {
           const uint32_t qb = ptx::smem_u32(&bars->q_full[qs]);
           ptx::mbar_arrive_expect_tx(qb, C::kTile);
           for (int hh = 0; hh < D / 64; ++hh)
-            ptx::tma_load_3d(sbase + C::kQ + qs * C::kTile + hh * 128 * 128, &tmQ, qb, hh * 64, i * BM, bhq);
+            ptx::tma_load_3d(sbase + C::kQ + qs * C::kTile + hh * 128 * 128, &tmQ, qb, hh * 64, row0 + i * BM, bhq);
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->o_empty[os]), ((uint32_t)(n / C::kOSlots) & 1u) ^ 1u,
                               lim_ms, a.err);
           if (ok) {
             const uint32_t ob = ptx::smem_u32(&bars->o_full[os]);
             ptx::mbar_arrive_expect_tx(ob, C::kTile);
             for (int hh = 0; hh < D / 64; ++hh)
-              ptx::tma_load_3d(sbase + C::kO + os * C::kTile + hh * 128 * 128, &tmDO, ob, hh * 64, i * BM, bhq);
+              ptx::tma_load_3d(sbase + C::kO + os * C::kTile + hh * 128 * 128, &tmDO, ob, hh * 64, row0 + i * BM, bhq);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -424,7 +436,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
       ptx::tc_fence_after();
     }
     const float mult = wg == 0 ? 1.f : a.scale;
-    uint16_t* out = static_cast<uint16_t*>(wg == 0 ? a.dv : a.dk) + ((size_t)bh * a.N + key) * D;
+    uint16_t* out = static_cast<uint16_t*>(wg == 0 ? a.dv : a.dk) + ((size_t)ks * a.rows + row0 + key) * D;
     const uint32_t src = wg == 0 ? C::kDV : C::kDK;
 #pragma unroll 1
     for (int hc = 0; hc < D / 32; ++hc) {
@@ -437,7 +449,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
 #pragma unroll
         for (int e = 0; e < 32; ++e) raw[e] = 0u;
       }
-      if (key < a.N) {
+      if (key < g.N) {
         uint4* dst = reinterpret_cast<uint4*>(out + hc * 32);
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4) {

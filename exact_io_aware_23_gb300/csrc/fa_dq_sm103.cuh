@@ -124,16 +124,27 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
   const int n_qt = (a.N + BM - 1) / BM;
   const int bh = a.heads_fastest ? unit % BH : unit / n_qt;
   const int it = a.heads_fastest ? unit / BH : unit % n_qt;
-  const int b = bh / a.H;
-  // grouped-query attention: query head h reads key/value head h / (H / Hkv)
-  const int bh_kv = b * a.Hkv + (bh % a.H) / (a.H / a.Hkv);
+  const int b = bh / a.H, h = bh % a.H;
   const uint32_t lim_ms = a.dbg.wait_limit_ms;
 
   Geo g;
   g.i = a.causal ? n_qt - 1 - it : it;
   g.q0 = g.i * BM;
-  g.N = a.N;
-  int kvl = a.N;
+  int row0 = 0, len = a.N;                       // this slice's rows on the token axis
+  if (a.cu_seqlens != nullptr) {
+    // Packed sequences: the grid is sized for the longest one; query tiles past this sequence's
+    // end have nothing to do, and offsets outside the contract are reported, not followed.
+    if (!packed_sequence(a.cu_seqlens, b, a.N, a.rows, &row0, &len)) {
+      if (threadIdx.x == 0) atomicExch(a.err, kDevBadOffsets);
+      return;
+    }
+    if (g.q0 >= len) return;
+  }
+  const int qs = a.cu_seqlens != nullptr ? h : bh;                              // Q, dO, dQ slice
+  // grouped-query attention: query head h reads key/value head h / (H / Hkv)
+  const int ks = (a.cu_seqlens != nullptr ? 0 : b * a.Hkv) + h / (a.H / a.Hkv);  // K, V slice
+  g.N = len;
+  int kvl = len;
   if (a.kv_lens != nullptr) kvl = max(0, min(a.N, (int)a.kv_lens[b]));
   g.kv_lim = kvl;
   g.causal = a.causal;
@@ -187,25 +198,25 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
       const uint32_t qb = ptx::smem_u32(&bars->q_full);
       ptx::mbar_arrive_expect_tx(qb, 2 * C::kTile);
       for (int hh = 0; hh < D / 64; ++hh) {
-        ptx::tma_load_3d(sbase + C::kQ + hh * 128 * 128, &tmQ, qb, hh * 64, g.q0, bh);
-        ptx::tma_load_3d(sbase + C::kDO + hh * 128 * 128, &tmDO, qb, hh * 64, g.q0, bh);
+        ptx::tma_load_3d(sbase + C::kQ + hh * 128 * 128, &tmQ, qb, hh * 64, row0 + g.q0, qs);
+        ptx::tma_load_3d(sbase + C::kDO + hh * 128 * 128, &tmDO, qb, hh * 64, row0 + g.q0, qs);
       }
       for (int j = g.next(0); j < g.j_end && ok; j = g.next(j + 1), ++n) {
-        const int ks = n % C::kKSlots, vs = n % C::kVSlots;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_empty[ks]), ((uint32_t)(n / C::kKSlots) & 1u) ^ 1u,
+        const int kslot = n % C::kKSlots, vslot = n % C::kVSlots;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_empty[kslot]), ((uint32_t)(n / C::kKSlots) & 1u) ^ 1u,
                             lim_ms, a.err);
         if (!ok) break;
-        const uint32_t kb = ptx::smem_u32(&bars->k_full[ks]);
+        const uint32_t kb = ptx::smem_u32(&bars->k_full[kslot]);
         ptx::mbar_arrive_expect_tx(kb, C::kTile);
         for (int hh = 0; hh < D / 64; ++hh)
-          ptx::tma_load_3d(sbase + C::kK + ks * C::kTile + hh * 128 * 128, &tmK, kb, hh * 64, j * BN, bh_kv);
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[vs]), ((uint32_t)(n / C::kVSlots) & 1u) ^ 1u,
+          ptx::tma_load_3d(sbase + C::kK + kslot * C::kTile + hh * 128 * 128, &tmK, kb, hh * 64, row0 + j * BN, ks);
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[vslot]), ((uint32_t)(n / C::kVSlots) & 1u) ^ 1u,
                             lim_ms, a.err);
         if (!ok) { ++n; break; }
-        const uint32_t vb = ptx::smem_u32(&bars->v_full[vs]);
+        const uint32_t vb = ptx::smem_u32(&bars->v_full[vslot]);
         ptx::mbar_arrive_expect_tx(vb, C::kTile);
         for (int hh = 0; hh < D / 64; ++hh)
-          ptx::tma_load_3d(sbase + C::kV + vs * C::kTile + hh * 128 * 128, &tmV, vb, hh * 64, j * BN, bh_kv);
+          ptx::tma_load_3d(sbase + C::kV + vslot * C::kTile + hh * 128 * 128, &tmV, vb, hh * 64, row0 + j * BN, ks);
       }
       // drain: copies in flight must land before shared memory is released
       ptx::mbar_wait(qb, 0, lim_ms, a.err);
@@ -235,12 +246,12 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
       if (any) {
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, lim_ms, a.err);
         for (int j = g.next(0); j < g.j_end && ok; j = g.next(j + 1), ++n) {
-          const int ks = n % C::kKSlots, vs = n % C::kVSlots;
-          ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_full[ks]), (uint32_t)(n / C::kKSlots) & 1u,
+          const int kslot = n % C::kKSlots, vslot = n % C::kVSlots;
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_full[kslot]), (uint32_t)(n / C::kKSlots) & 1u,
                               lim_ms, a.err);
           if (!ok) break;
           ptx::tc_fence_after();
-          const uint32_t sk = sbase + C::kK + ks * C::kTile;
+          const uint32_t sk = sbase + C::kK + kslot * C::kTile;
           // S(n) = Q K_j^T (K-major operands, k-steps of 16 along d).  Its buffer last held
           // dS(n-2), read by dQ(n-2), which was issued before this.
           const uint32_t sb = C::kS + (uint32_t)(n & 1) * 128;
@@ -260,11 +271,11 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
             ptx::mma_commit(ptx::smem_u32(&bars->k_empty[(n - 1) % C::kKSlots]));
           }
           // dP(n) = dO V_j^T; V_j is free once this product is done
-          ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_full[vs]), (uint32_t)(n / C::kVSlots) & 1u,
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_full[vslot]), (uint32_t)(n / C::kVSlots) & 1u,
                               lim_ms, a.err);
           if (!ok) break;
           ptx::tc_fence_after();
-          const uint32_t sv = sbase + C::kV + vs * C::kTile;
+          const uint32_t sv = sbase + C::kV + vslot * C::kTile;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
@@ -272,7 +283,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
                         ptx::sdesc_sw128(sv + off, 16, 1024), C::kIdescS, kk > 0);
           }
           ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
-          ptx::mma_commit(ptx::smem_u32(&bars->v_empty[vs]));
+          ptx::mma_commit(ptx::smem_u32(&bars->v_empty[vslot]));
         }
         if (ok && n > 0) {
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_ready), (uint32_t)(n - 1) & 1u, lim_ms, a.err);
@@ -294,11 +305,11 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
     const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
     const float c = a.scale * kLog2e;
     const float2 c2 = make_float2(c, c);
-    const size_t row = (size_t)bh * a.N + q;
-    float L = q < a.N ? a.lse[row] : -INFINITY;
+    const size_t row = (size_t)qs * a.rows + row0 + q;
+    float L = q < g.N ? a.lse[row] : -INFINITY;
     const float nl = L == -INFINITY ? -INFINITY : -L * kLog2e;   // P vanishes on empty rows
     const float2 nl2 = make_float2(nl, nl);
-    const float dd = q < a.N ? a.delta[row] : 0.f;
+    const float dd = q < g.N ? a.delta[row] : 0.f;
     const float2 dd2 = make_float2(dd, dd);
     bool ok = true;
     int n = 0;
@@ -385,7 +396,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
 #pragma unroll
         for (int e = 0; e < 32; ++e) raw[e] = 0u;
       }
-      if (q < a.N) {
+      if (q < g.N) {
         uint4* dst = reinterpret_cast<uint4*>(out + hc * 32);
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4) {

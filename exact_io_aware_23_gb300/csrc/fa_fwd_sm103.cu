@@ -70,6 +70,8 @@ static_assert(sizeof(Bars) <= 256, "the live-tile bitmap starts 256 bytes after 
 // Per-CTA tile geometry: which key tiles exist and how each Q tile must treat them.
 struct Geo {
   int bh;          // (b, h) slice
+  int row0;        // first row of the slice on the token axis (packed sequences; else 0)
+  int qs, ks;      // slice index of Q/O and of K/V in the tensor maps and row arithmetic
   int split;       // key-tile range (split-KV)
   int j0;          // first key tile of this CTA's range
   int q0;          // first query row of Q tile 0
@@ -131,20 +133,29 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int bh = a.heads_fastest ? unit % BH : unit / n_pairs;
     const int slot = a.heads_fastest ? unit / BH : unit % n_pairs;
     const int pair = a.causal ? n_pairs - 1 - slot : slot;
-    const int b = bh / a.H;
+    const int b = bh / a.H, h = bh % a.H;
     Geo g;
     g.bh = bh;
     g.split = split;
     g.q0 = pair * 2 * BM;
     g.N = a.N;
+    g.row0 = 0;
     int kvl = a.Nk;
+    if (a.cu_seqlens != nullptr) {                 // packed: this sequence's rows of head h
+      int len = 0;
+      if (!packed_sequence(a.cu_seqlens, b, a.N, a.rows, &g.row0, &len)) g.row0 = -1;
+      g.N = kvl = len;
+    }
+    g.qs = a.cu_seqlens != nullptr ? h : bh;
+    // grouped-query attention: query head h reads key/value head h / (H / Hkv)
+    g.ks = (a.cu_seqlens != nullptr ? 0 : b * a.Hkv) + h / (a.H / a.Hkv);
     if (a.kv_lens != nullptr) kvl = max(0, min(a.Nk, (int)a.kv_lens[b]));
     g.kv_lim = kvl;
     g.causal = a.causal;
     g.bm = a.block_mask;
     g.T = a.n_tiles;
     int last_key = g.kv_lim;
-    if (a.causal) last_key = min(last_key, min(g.q0 + 2 * BM, a.N));
+    if (a.causal) last_key = min(last_key, min(g.q0 + 2 * BM, g.N));
     g.j_end = (last_key + BN - 1) / BN;
     g.j0 = 0;
     if (a.n_splits > 1) {
@@ -155,6 +166,16 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     return g;
   };
   const uint32_t lim_ms = a.dbg.wait_limit_ms;
+  if (a.cu_seqlens != nullptr) {
+    // Packed sequences: the grid is sized for the longest one; tiles past this sequence's end
+    // have nothing to do, and offsets outside the contract are reported, not followed.
+    const Geo g0 = make_geo();
+    if (g0.row0 < 0) {
+      if (threadIdx.x == 0) atomicExch(a.err, kDevBadOffsets);
+      return;
+    }
+    if (g0.q0 >= g0.N) return;
+  }
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
@@ -192,9 +213,6 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (warp >= 8) {
     ptx::regs_dec<88>();
     const Geo g = make_geo();
-    const int bh = g.bh;
-    // grouped-query attention: query head h reads key/value head h / (H / Hkv)
-    const int bh_kv = (bh / a.H) * a.Hkv + (bh % a.H) / (a.H / a.Hkv);
     if (warp == 8 && lane == 0) {
       // ------------------------------- TMA producer -------------------------------------------
       ptx::tma_prefetch_desc(&tmQ);
@@ -204,7 +222,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       ptx::mbar_arrive_expect_tx(qbar, 2 * C::kTileBytes);
       for (int t = 0; t < 2; ++t)
         for (int hh = 0; hh < D / 64; ++hh)
-          ptx::tma_load_3d(sQ + t * C::kTileBytes + hh * BM * 128, &tmQ, qbar, hh * 64, g.q0 + t * BM, bh);
+          ptx::tma_load_3d(sQ + t * C::kTileBytes + hh * BM * 128, &tmQ, qbar, hh * 64, g.row0 + g.q0 + t * BM, g.qs);
       int n = 0;
       bool ok = true;
       for (int j = g.next(g.j0); j < g.j_end && ok; j = g.next(j + 1)) {
@@ -218,7 +236,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
           const CUtensorMap* m = kind == 0 ? &tmK : &tmV;
           for (int hh = 0; hh < D / 64; ++hh)
-            ptx::tma_load_3d(sKV + slot * C::kTileBytes + hh * BN * 128, m, fb, hh * 64, j * BN, bh_kv);
+            ptx::tma_load_3d(sKV + slot * C::kTileBytes + hh * BN * 128, m, fb, hh * 64, g.row0 + j * BN, g.ks);
         }
       }
       // Drain: every copy this CTA issued must have landed before shared memory is released.
@@ -302,7 +320,6 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // ------------------------------- softmax warpgroups -----------------------------------------
     ptx::regs_inc<200>();
     const Geo g = make_geo();
-    const int bh = g.bh;
     const int t = warp / 4;
     const int sub = warp % 4;
     const int r = sub * 32 + lane;                  // TMEM lane == row within the Q tile
@@ -406,9 +423,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
     const bool any = l_run > 0.f;
     const float inv = any ? 1.f / l_run : 0.f;
-    uint16_t* orow = static_cast<uint16_t*>(a.o) + ((size_t)bh * a.N + i) * D;
+    const size_t row = (size_t)g.qs * a.rows + g.row0 + i;      // this query row on its axis
+    uint16_t* orow = static_cast<uint16_t*>(a.o) + row * D;
     // split-KV: this range's normalised partial output (fp32) and log-sum-exp
-    const size_t prow = ((size_t)g.split * a.B * a.H + bh) * a.N + i;
+    const size_t prow = (size_t)g.split * a.B * a.H * a.N + row;
     float* porow = a.o_part != nullptr ? a.o_part + prow * D : nullptr;
 #pragma unroll 1
     for (int q4 = 0; q4 < D / 32; ++q4) {
@@ -421,13 +439,13 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = 0u;
       }
-      if (i < a.N && porow != nullptr) {
+      if (i < g.N && porow != nullptr) {
         float4* dst = reinterpret_cast<float4*>(porow + q4 * 32);
 #pragma unroll
         for (int v4 = 0; v4 < 8; ++v4)
           dst[v4] = make_float4(__uint_as_float(o[4 * v4 + 0]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
                                 __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
-      } else if (i < a.N) {
+      } else if (i < g.N) {
         uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4) {
@@ -440,10 +458,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
     }
-    if (i < a.N) {
+    if (i < g.N) {
       const float L = any ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
       if (porow != nullptr) a.lse_part[prow] = L;
-      else a.lse[(size_t)bh * a.N + i] = L;
+      else a.lse[row] = L;
     }
   }
 
@@ -467,11 +485,13 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH, boo
 template <int D, bool F16>
 cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
-  const int BH = a.B * a.H;
+  // token axis and slice count of the tensor maps: per (b, h) slice, or packed per head
+  const bool packed = a.cu_seqlens != nullptr;
+  const int q_slices = packed ? a.H : a.B * a.H, kv_slices = packed ? a.Hkv : a.B * a.Hkv;
   cudaError_t e;
-  if ((e = make_map(&mq, a.q, D, a.N, BH, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, a.k, D, a.Nk, a.B * a.Hkv, F16)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, a.v, D, a.Nk, a.B * a.Hkv, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mq, a.q, D, a.rows, q_slices, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, a.k, D, packed ? a.rows : a.Nk, kv_slices, F16)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.v, D, packed ? a.rows : a.Nk, kv_slices, F16)) != cudaSuccess) return e;
   auto kern = fwd_sm103_kernel<D, F16>;
   // + the live-tile bitmap of a block-sparse mask (one bit per key tile)
   const int smem = Cfg<D, F16>::kSmem + (a.block_mask != nullptr ? ((a.n_tiles + 127) / 128) * 16 : 0);
@@ -482,7 +502,7 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   cudaFuncAttributes fattr;
   if ((e = cudaFuncGetAttributes(&fattr, kern)) != cudaSuccess) return e;
   if (fattr.numRegs * kThreads < 128 * 88 + 256 * 200) return cudaErrorInvalidConfiguration;
-  dim3 grid(((a.N + 2 * BM - 1) / (2 * BM)) * BH * a.n_splits);
+  dim3 grid(((a.N + 2 * BM - 1) / (2 * BM)) * a.B * a.H * a.n_splits);
   kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }

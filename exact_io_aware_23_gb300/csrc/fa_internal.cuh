@@ -12,7 +12,7 @@ namespace fa {
 constexpr int kMaskTile = 128;   // granularity of the block-sparse tile mask
 
 // Error word written by kernels (one per device, read by fa_check_device_status).
-enum DeviceError : int { kDevOk = 0, kDevTimeout = 1 };
+enum DeviceError : int { kDevOk = 0, kDevTimeout = 1, kDevMisaligned = 2, kDevBadOffsets = 3 };
 
 struct DebugKnobs {
   int inject;              // 1: skip the first K/V tile load of every CTA (watchdog test)
@@ -43,6 +43,11 @@ struct FwdArgs {
   int tiles_per_split;
   float* o_part;
   float* lse_part;
+  // Packed sequences (ragged offsets): null, or [B + 1] device offsets of B sequences packed
+  // back to back along each head's token axis of `rows` tokens; N is then the longest
+  // sequence and Q, K, V, O are [H or Hkv, rows, d].  Without them rows = N.
+  const int32_t* cu_seqlens;
+  int rows;
 };
 
 struct SplitMergeArgs {       // combines the split-KV partials with the (m, l, u) merge law
@@ -77,7 +82,24 @@ struct BwdArgs {
   int* err;
   DebugKnobs dbg;
   int heads_fastest;          // launch order: (b, h) slice fastest (unequal work per tile)
+  const int32_t* cu_seqlens;  // packed sequences, as in FwdArgs
+  int rows;
 };
+
+// Rows of the query-side tensors (Q, O, dO, dQ, LSE, D) over all slices.
+__host__ __device__ inline size_t q_rows_total(const BwdArgs& a) {
+  return a.cu_seqlens != nullptr ? (size_t)a.H * a.rows : (size_t)a.B * a.H * a.N;
+}
+
+// One packed sequence: its first row on the token axis and its length; false when the offsets
+// break the documented contract (then nothing of that sequence is read or written).
+__device__ __forceinline__ bool packed_sequence(const int32_t* cu, int b, int max_len, int rows,
+                                                int* row0, int* len) {
+  const int r0 = cu[b], r1 = cu[b + 1];
+  *row0 = r0;
+  *len = r1 - r0;
+  return r0 >= 0 && r1 >= r0 && r1 - r0 <= max_len && r1 <= rows;
+}
 
 // CUDA-core (SIMT) kernels: the fp32 path.
 cudaError_t launch_fwd_simt(const FwdArgs& a, fa_dtype dt, cudaStream_t s);

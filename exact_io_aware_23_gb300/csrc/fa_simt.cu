@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(BwdArgs a) {
 // One warp per row.
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) bwd_preprocess_kernel(BwdArgs a) {
-  const size_t rows = (size_t)a.B * a.H * a.N;
+  const size_t rows = q_rows_total(a);
   const size_t row = (size_t)blockIdx.x * (kThreads / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (row >= rows) return;
@@ -395,7 +395,7 @@ cudaError_t bwd_launch(const BwdArgs& a, cudaStream_t s) {
 
 template <typename T, int D>
 cudaError_t pre_launch(const BwdArgs& a, cudaStream_t s) {
-  const size_t rows = (size_t)a.B * a.H * a.N;
+  const size_t rows = q_rows_total(a);
   const size_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
   bwd_preprocess_kernel<T, D><<<(unsigned)blocks, kThreads, 0, s>>>(a);
   return cudaGetLastError();
@@ -403,7 +403,7 @@ cudaError_t pre_launch(const BwdArgs& a, cudaStream_t s) {
 
 template <typename T>
 cudaError_t conv_launch(const BwdArgs& a, cudaStream_t s) {
-  const size_t n = (size_t)a.B * a.H * a.N * a.d;
+  const size_t n = q_rows_total(a) * a.d;
   size_t blocks = (n + kThreads - 1) / kThreads;
   if (blocks > 152 * 16) blocks = 152 * 16;
   bwd_dq_convert_kernel<T><<<(unsigned)blocks, kThreads, 0, s>>>(a, n);

@@ -118,6 +118,32 @@ fa_status fa_backward_deterministic(const void* q, const void* k, const void* v,
                                     size_t workspace_bytes, void* stream);
 
 /*
+ * Packed sequences ("ragged offsets" and the "document mask" in the pages' list of production
+ * semantics, "FlashAttention：让精确注意力服从内存层次", list after the CPU reference).  n_seqs
+ * sequences of different lengths are stored back to back along each head's token axis:
+ *   q, o, dO, dq : [H, total, d];  k, v, dk, dv : [Hkv, total, d];  lse : fp32 [H, total]
+ *   cu_seqlens   : device int32 [n_seqs + 1], 0 = cu[0] <= cu[1] <= ... <= cu[n_seqs] <= total;
+ *                  sequence s is rows [cu[s], cu[s+1]) of every head
+ *   max_seqlen   : an upper bound of every cu[s+1] - cu[s] (sizes the grid; host value)
+ * A query attends only to keys of its own sequence (and, with causal, to those at or before it
+ * within the sequence); rows outside every sequence are neither read into a result nor written.
+ * Grouped heads as in fa_forward_gqa.  bf16 or fp16 only.  The backward is the two-pass
+ * backward of fa_backward_deterministic; its workspace is
+ * fa_backward_deterministic_workspace_size(1, H, total) bytes.  The offsets live on the device,
+ * so they are checked there: a sequence whose offsets break the rules above is skipped and
+ * fa_check_device_status then returns FA_ERR_INVALID_ARG.
+ */
+fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int32_t* cu_seqlens, int n_seqs, int max_seqlen, int total,
+                            int H, int Hkv, int d, float scale, int causal, fa_dtype dtype,
+                            void* stream);
+fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const void* o,
+                             const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                             const int32_t* cu_seqlens, int n_seqs, int max_seqlen, int total,
+                             int H, int Hkv, int d, float scale, int causal, fa_dtype dtype,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Split-KV forward for decode-shaped problems (few queries against a long key sequence) and for
  * problems with too few (b, h) slices to fill the GPU: the key tiles of every query tile are cut
  * into n_splits ranges processed by separate CTAs, each producing its own (O_s, LSE_s); a merge
@@ -195,8 +221,9 @@ size_t fa_backward_noalloc_max_workspace(void);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error word.  Returns
- * FA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last check, FA_ERR_CUDA if
- * the synchronisation reported a CUDA error, FA_OK otherwise.
+ * FA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last check, FA_ERR_INVALID_ARG
+ * if a kernel found packed-sequence offsets outside their contract, FA_ERR_CUDA if the
+ * synchronisation reported a CUDA error, FA_OK otherwise.
  */
 fa_status fa_check_device_status(void* stream);
 

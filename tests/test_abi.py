@@ -179,3 +179,31 @@ def test_backward_variant_selector(lib):
     assert lib.fa_set_backward_variant(-1) == INVALID
     assert lib.fa_set_backward_variant(1) == OK
     assert lib.fa_set_backward_variant(0) == OK           # back to the default
+
+
+def test_varlen_argument_checks(lib):
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_forward_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
+    lib.fa_backward_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
+                                       i, i, vp, sz, vp]
+    lib.fa_backward_deterministic_workspace_size.argtypes = [i, i, i]
+    lib.fa_backward_deterministic_workspace_size.restype = sz
+    ws = lib.fa_backward_deterministic_workspace_size(1, 8, 1000)
+
+    def fwd_v(cu=P, S=3, maxl=500, T=1000, H=8, Hkv=2, dtype=0, d=64):
+        return lib.fa_forward_varlen(P, P, P, P, P, cu, S, maxl, T, H, Hkv, d, 0.125, 1, dtype, None)
+
+    def bwd_v(cu=P, S=3, maxl=500, T=1000, H=8, Hkv=2, dtype=0, wsb=ws):
+        return lib.fa_backward_varlen(P, P, P, P, P, P, P, P, P, cu, S, maxl, T, H, Hkv, 64, 0.125,
+                                      1, dtype, P, wsb, None)
+    for call in (fwd_v, bwd_v):
+        assert call(dtype=1) == UNSUPPORTED          # fp32 has no packed path
+        assert call(Hkv=3) == UNSUPPORTED
+        assert call(cu=None) == INVALID
+        assert call(S=-1) == INVALID
+        assert call(T=-1) == INVALID
+        assert call(maxl=-1) == INVALID
+        assert call(T=0) == OK                       # nothing packed: no-op
+        assert call(S=0, cu=None) == OK
+    assert fwd_v(d=80) == UNSUPPORTED
+    assert bwd_v(wsb=ws - 4) == INVALID
