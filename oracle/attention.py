@@ -46,6 +46,11 @@ What it computes, and where the pages fix it:
   document mask), and with ``causal`` only to keys at or before it.  Packed this way, B = 1 and
   N = total.
 
+* Dropout on P (same list: "dropout RNG"; the numerics section asks for the dropout replay to
+  be tested): ``dropout=(seed, offset, k8)`` applies the mask of ``oracle.dropout`` (Philox
+  counter-based, so the backward regenerates it) as O = (P * M * 256/k8) V; LSE is that of the
+  undropped scores; the backward uses the same mask.  See ``oracle/dropout.py`` for the reading.
+
 Large inputs are processed a chunk of query rows at a time (a memory bound only: each chunk
 still forms its full score rows).  When a tile mask removes most columns, a chunk gathers
 the columns that any of its rows may attend to; every other column is masked for the whole
@@ -57,6 +62,8 @@ import math
 from typing import Optional, Sequence
 
 import numpy as np
+
+from . import dropout as _dropout
 
 TILE = 128          # block-mask granularity (score tiles of 128 x 128)
 ROW_CHUNK = 1024    # query rows per chunk (bounds the size of one score block)
@@ -137,9 +144,17 @@ def _check_segments(segments, B: int, N: int, kv_lens):
         raise ValueError("packed sequences need B = 1, no kv_lens and offsets 0 <= ... <= N = total")
 
 
+def _drop(dropout, r, cols, bh):
+    """(mask-and-scale factor [len(r), len(cols)]) of the dropout reading, or None."""
+    if dropout is None:
+        return None
+    seed, offset, k8 = dropout
+    return _dropout.keep_mask(r, cols, bh, seed, offset, k8) * _dropout.scale_of(k8)
+
+
 def forward(q, k, v, scale: float, causal: bool = False, kv_lens=None, block_mask=None,
             rows: Optional[Sequence[int]] = None, heads: Optional[Sequence[int]] = None,
-            segments=None):
+            segments=None, dropout=None):
     """Dense masked attention in fp64.
 
     q: float64 array [B, H, N, d]; k, v: [B, Hkv, N, d] with Hkv dividing H (query head h reads
@@ -147,7 +162,8 @@ def forward(q, k, v, scale: float, causal: bool = False, kv_lens=None, block_mas
     a different N only when neither causal nor a block mask is set.  Returns
     (O [B,H,R,d], LSE [B,H,R]) for the R query rows in ``rows`` (default: all rows) and the
     heads in ``heads`` (default: all heads).  ``segments``: offsets of packed sequences along
-    the token axis (B = 1); a query sees only the keys of its own sequence.
+    the token axis (B = 1); a query sees only the keys of its own sequence.  ``dropout``:
+    (seed, offset, k8) of ``oracle.dropout`` (not combined with ``segments``).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -155,6 +171,8 @@ def forward(q, k, v, scale: float, causal: bool = False, kv_lens=None, block_mas
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
     _check_segments(segments, B, Nq, kv_lens)
+    if dropout is not None and segments is not None:
+        raise ValueError("dropout with packed sequences is not part of this reading")
     rows = np.arange(Nq) if rows is None else np.asarray(rows, dtype=np.int64)
     heads = list(range(H)) if heads is None else list(heads)
     lens = _as_i64_list(kv_lens, B)
@@ -171,6 +189,9 @@ def forward(q, k, v, scale: float, causal: bool = False, kv_lens=None, block_mas
                 s = _scores(q[b, h, r], k[b, g, cols], scale, ok)
                 lse = _row_lse(s)
                 p = _probs(s, lse)
+                mk = _drop(dropout, r, cols, b * H + h)
+                if mk is not None:
+                    p = p * mk
                 O[b, hi, c0:c0 + r.size] = p @ v[b, g, cols]
                 L[b, hi, c0:c0 + r.size] = lse
     return O, L
@@ -187,13 +208,14 @@ def probabilities(q, k, scale: float, causal: bool = False, kv_len=None, block_m
 
 def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, block_mask=None,
              heads: Optional[Sequence[int]] = None, return_delta: bool = False,
-             rows: Optional[Sequence[int]] = None, o=None, segments=None):
+             rows: Optional[Sequence[int]] = None, o=None, segments=None, dropout=None):
     """Explicit-gradient backward of dense masked attention, fp64.
 
     Returns (dQ, dK, dV), each [B, len(heads), N, d]; with ``return_delta`` also D [B,H',N].
     With fewer key/value heads than query heads (k, v [B, Hkv, N, d]; see ``forward``), dK and
     dV are [B, Hkv, N, d] and each key/value head sums the contributions of the selected query
-    heads that read it.  ``segments`` as in ``forward``.
+    heads that read it.  ``segments`` and ``dropout`` as in ``forward``: with dropout,
+    dV = (P * M * s)^T dO and dP = (dO V^T) * M * s (s = 256 / k8), D and dS as without it.
     D_i = sum_j P_ij dP_ij, the exact gradient's row term.  When the forward output ``o``
     ([B,H,N,d]) is given, D_i = sum_c dO_ic o_ic instead: the backward as an operator of its
     inputs (q, k, v, o, dO, LSE), the form the method's backward takes (equal to the first
@@ -207,6 +229,8 @@ def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, bloc
     do = np.asarray(do, dtype=np.float64)
     B, H, N, d = q.shape
     _check_segments(segments, B, N, kv_lens)
+    if dropout is not None and segments is not None:
+        raise ValueError("dropout with packed sequences is not part of this reading")
     heads = list(range(H)) if heads is None else list(heads)
     lens = _as_i64_list(kv_lens, B)
     Hkv = k.shape[1]
@@ -227,6 +251,10 @@ def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, bloc
                 s = _scores(q[b, h, r], k[b, g, cols], scale, ok)
                 p = _probs(s, _row_lse(s))
                 dp = do[b, h, r] @ v[b, g, cols].T
+                mk = _drop(dropout, r, cols, b * H + h)
+                pd = p if mk is None else p * mk           # the probabilities O was built from
+                if mk is not None:
+                    dp = dp * mk
                 if o is None:
                     D = (p * dp).sum(axis=1)
                 else:
@@ -234,7 +262,7 @@ def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, bloc
                 ds = p * (dp - D[:, None])
                 dQ[b, hi, r] = scale * (ds @ k[b, g, cols])
                 dK[b, kvi, cols] += scale * (ds.T @ q[b, h, r])
-                dV[b, kvi, cols] += p.T @ do[b, h, r]
+                dV[b, kvi, cols] += pd.T @ do[b, h, r]
                 Dd[b, hi, r] = D
     if return_delta:
         return dQ, dK, dV, Dd

@@ -434,6 +434,108 @@ def test_packed_sequences_finite_differences():
             assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(g[idx])), (name, idx, fd, g[idx])
 
 
+# --- dropout (counter-based mask, replayed in the backward) ---------------------------------
+
+from oracle import dropout as odrop
+
+
+def test_philox_known_answers():
+    """The generator reproduces its authors' published known-answer vectors."""
+    path = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.json")
+    for vec in json.load(open(path))["vectors"]:
+        ctr = np.array([int(x, 16) for x in vec["counter"]], dtype=np.uint64)
+        key = np.array([int(x, 16) for x in vec["key"]], dtype=np.uint64)
+        out = odrop.philox4x32_10(ctr, key)
+        assert [int(x) for x in out] == [int(x, 16) for x in vec["out"]]
+
+
+def test_dropout_uniform_layout():
+    """u(i, j) is byte (j mod 4) of word (i mod 4) of the call at counter
+    (j // 4, i // 4, b*H + h, offset), key (seed low, seed high)."""
+    seed, off, bh = 0x0123456789ABCDEF, 7, 3
+    u = odrop.uniforms(np.arange(12), np.arange(20), bh, seed, off)
+    for i, j in ((0, 0), (5, 6), (11, 19), (3, 16), (8, 3)):
+        w = odrop.philox4x32_10(np.array([j // 4, i // 4, bh, off], dtype=np.uint64),
+                                np.array([seed & 0xFFFFFFFF, seed >> 32], dtype=np.uint64))
+        assert u[i, j] == (int(w[i % 4]) >> (8 * (j % 4))) & 0xFF
+
+
+@pytest.mark.parametrize("p", [0.1, 0.5, 0.9])
+def test_dropout_keep_fraction_and_flat_bytes(p):
+    k8 = odrop.keep_threshold(p)
+    assert k8 == round((1 - p) * 256)
+    u = odrop.uniforms(np.arange(512), np.arange(512), 5, 1234 + k8, 0).astype(np.int64)
+    n = u.size
+    kept = (u < k8).mean()
+    assert abs(kept - k8 / 256) <= 4 * np.sqrt(k8 / 256 * (1 - k8 / 256) / n)
+    hist = np.bincount(u.ravel(), minlength=256)
+    chi2 = ((hist - n / 256) ** 2 / (n / 256)).sum()
+    assert chi2 < 255 + 6 * np.sqrt(2 * 255)          # about six sigma above its mean
+
+
+def test_dropout_rate_zero_is_plain_attention():
+    q, k, v, do = (_rand((1, 2, 70, 8), s) for s in (200, 201, 202, 203))
+    O, L = oracle.forward(q, k, v, 0.3, causal=True)
+    O2, L2 = oracle.forward(q, k, v, 0.3, causal=True, dropout=(99, 3, 256))
+    assert np.array_equal(O, O2) and np.array_equal(L, L2)
+    g = oracle.backward(q, k, v, do, 0.3, causal=True)
+    g2 = oracle.backward(q, k, v, do, 0.3, causal=True, dropout=(99, 3, 256))
+    assert all(np.array_equal(a, b) for a, b in zip(g, g2))
+
+
+def test_dropout_everything_dropped():
+    q, k, v, do = (_rand((1, 1, 40, 4), s) for s in (210, 211, 212, 213))
+    O, L = oracle.forward(q, k, v, 0.5, dropout=(5, 0, 0))
+    L0 = oracle.forward(q, k, v, 0.5)[1]
+    assert np.count_nonzero(O) == 0 and np.array_equal(L, L0)     # LSE is the undropped one
+    dQ, dK, dV = oracle.backward(q, k, v, do, 0.5, dropout=(5, 0, 0))
+    assert np.count_nonzero(dQ) == np.count_nonzero(dK) == np.count_nonzero(dV) == 0
+
+
+def test_dropout_is_unbiased():
+    """Averaged over many seeds, the dropped-out output approaches the plain output (inverted
+    dropout keeps the expectation)."""
+    q, k, v = (_rand((1, 1, 12, 3), s) for s in (220, 221, 222))
+    O = oracle.forward(q, k, v, 0.7)[0]
+    k8 = odrop.keep_threshold(0.3)
+    acc = np.zeros_like(O)
+    n = 400
+    for seed in range(n):
+        acc += oracle.forward(q, k, v, 0.7, dropout=(seed, 0, k8))[0]
+    err = np.abs(acc / n - O).max()
+    spread = np.abs(O).max() * np.sqrt((256 - k8) / k8 / n)
+    assert err < 4 * spread
+
+
+def test_dropout_backward_finite_differences():
+    """With the mask fixed by (seed, offset), the function is smooth in q, k, v: the gradients
+    match central differences."""
+    drop = (77, 2, odrop.keep_threshold(0.25))
+    q, k, v, do = (_rand((1, 2, 9, 3), s, 1.1) for s in (230, 231, 232, 233))
+    dQ, dK, dV = oracle.backward(q, k, v, do, 0.6, causal=True, dropout=drop)
+    h = 1e-6
+    for name, x, g in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+        for f in range(x.size):
+            idx = tuple(int(i) for i in np.unravel_index(f, x.shape))
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args = {"q": q, "k": k, "v": v}
+            lp = _loss(**{**args, name: xp}, do=do, scale=0.6, causal=True, dropout=drop)
+            lm = _loss(**{**args, name: xm}, do=do, scale=0.6, causal=True, dropout=drop)
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(g[idx])), (name, idx, fd, g[idx])
+
+
+def test_dropout_delta_both_ways():
+    """With dropout, sum_j P_ij dP_ij (dP with the mask) still equals rowsum(dO * O)."""
+    q, k, v, do = (_rand((1, 2, 150, 8), s) for s in (240, 241, 242, 243))
+    drop = (3, 9, odrop.keep_threshold(0.4))
+    O, _ = oracle.forward(q, k, v, 0.35, dropout=drop)
+    _, _, _, D = oracle.backward(q, k, v, do, 0.35, dropout=drop, return_delta=True)
+    assert np.max(np.abs(D - (do * O).sum(-1))) < 1e-12
+
+
 def test_backward_delta_both_ways_and_sums():
     """D_i = sum_j P_ij dP_ij equals rowsum(dO * O); sum_j dK_j = 0; sum_j dV_j = sum_i dO_i."""
     B, H, N, d = 1, 2, 200, 8

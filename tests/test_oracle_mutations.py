@@ -16,7 +16,7 @@ MUTATIONS = [
     ("dQ[b, hi, r] = scale * (ds @ k[b, g, cols])", "dQ[b, hi, r] = (ds @ k[b, g, cols])"),
     ("ds = p * (dp - D[:, None])", "ds = p * (dp + D[:, None])"),
     ("dK[b, kvi, cols] += scale * (ds.T @ q[b, h, r])", "dK[b, kvi, cols] += scale * (ds @ q[b, h, r])"),
-    ("dV[b, kvi, cols] += p.T @ do[b, h, r]", "dV[b, kvi, cols] += p.T @ do[b, h, r] * 1.0001"),
+    ("dV[b, kvi, cols] += pd.T @ do[b, h, r]", "dV[b, kvi, cols] += pd.T @ do[b, h, r] * 1.0001"),
     ("ok &= cols[None, :] <= rows[:, None]", "ok &= cols[None, :] < rows[:, None]"),
     ("ok &= (cols < kv_len)[None, :]", "ok &= (cols <= kv_len)[None, :]"),
     ("ok &= bm[(rows // TILE)[:, None], (cols // TILE)[None, :]]",
@@ -34,6 +34,12 @@ MUTATIONS = [
     ("kvi = g if grouped else hi", "kvi = hi % Hkv if grouped else hi"),
     ('return np.searchsorted(np.asarray(segments, dtype=np.int64), x, side="right") - 1',
      'return np.searchsorted(np.asarray(segments, dtype=np.int64), x, side="left") - 1'),
+    ("return ((w >> (8 * (J & 3)).astype(np.uint32)) & 0xFF).astype(np.uint8)",
+     "return ((w >> (8 * (I & 3)).astype(np.uint32)) & 0xFF).astype(np.uint8)"),
+    ("return 256.0 / k8 if k8 > 0 else 0.0", "return 255.0 / k8 if k8 > 0 else 0.0"),
+    ("                    dp = dp * mk\n", "                    dp = dp\n"),
+    ("        c0, c1, c2, c3 = hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0",
+     "        c0, c1, c2, c3 = hi1 ^ c1 ^ k1, lo1, hi0 ^ c3 ^ k0, lo0"),
 ]
 
 
@@ -58,9 +64,11 @@ def test_clean_copy_passes(sandbox):
 
 @pytest.mark.parametrize("old,new", MUTATIONS, ids=[m[1][:40] for m in MUTATIONS])
 def test_planted_mistake_is_caught(sandbox, old, new):
-    path = sandbox / "oracle" / "attention.py"
-    src = open(os.path.join(ROOT, "oracle", "attention.py")).read()
-    assert old in src
+    old, new = old.replace("\\n", "\n"), new.replace("\\n", "\n")
+    name = next(f for f in ("attention.py", "dropout.py")
+                if old in open(os.path.join(ROOT, "oracle", f)).read())
+    path = sandbox / "oracle" / name
+    src = open(os.path.join(ROOT, "oracle", name)).read()
     path.write_text(src.replace(old, new))
     try:
         r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", "tests/test_oracle.py"],
