@@ -24,6 +24,11 @@ FA_BF16, FA_FP32, FA_FP16 = 0, 1, 2
 _DTYPES = {torch.bfloat16: FA_BF16, torch.float32: FA_FP32, torch.float16: FA_FP16}
 
 
+class FaDropout(ctypes.Structure):
+    """fa_dropout: dropout probability, generator key and counter offset."""
+    _fields_ = [("p", ctypes.c_float), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint32)]
+
+
 class FaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -67,6 +72,12 @@ def _load() -> ctypes.CDLL:
     L.fa_backward_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
                                      i, i, vp, sz, vp]
     L.fa_backward_varlen.restype = i
+    dp = ctypes.POINTER(FaDropout)
+    L.fa_forward_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, dp, vp]
+    L.fa_forward_dropout.restype = i
+    L.fa_backward_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i,
+                                      vp, dp, vp, sz, vp]
+    L.fa_backward_dropout.restype = i
     L.fa_set_backward_variant.argtypes = [i]
     L.fa_set_backward_variant.restype = i
     L.fa_forward_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, i, vp, sz, vp]
@@ -130,14 +141,24 @@ def _masks(block_mask, kv_lens, B, N, device):
 def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = False,
             scale: Optional[float] = None, block_mask: Optional[torch.Tensor] = None,
             kv_lens: Optional[torch.Tensor] = None, o: Optional[torch.Tensor] = None,
-            lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """O, LSE = attention forward (fa_forward; fa_forward_gqa when k, v have fewer heads).
-    q: [B, H, N, d]; k, v: [B, Hkv, N, d]; bf16, fp16 or fp32 on CUDA."""
+            lse: Optional[torch.Tensor] = None, stream=None, dropout_p: float = 0.0,
+            seed: int = 0, offset: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
+    """O, LSE = attention forward (fa_forward; fa_forward_gqa when k, v have fewer heads;
+    fa_forward_dropout when dropout_p > 0).  q: [B, H, N, d]; k, v: [B, Hkv, N, d]; bf16, fp16
+    or fp32 on CUDA."""
     B, H, N, d, Hkv = _check_qkv(q, k, v)
     scale = 1.0 / d ** 0.5 if scale is None else float(scale)
     block_mask, kv_lens = _masks(block_mask, kv_lens, B, N, q.device)
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if dropout_p > 0.0:
+        drop = FaDropout(float(dropout_p), int(seed), int(offset))
+        st = lib.fa_forward_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
+                                    scale, int(bool(causal)), _ptr(block_mask), _DTYPES[q.dtype],
+                                    _ptr(kv_lens), ctypes.byref(drop), _stream(stream))
+        if st != FA_OK:
+            raise FaError(st, "fa_forward_dropout")
+        return o, lse
     if Hkv == H:
         st = lib.fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
                             int(bool(causal)), _ptr(block_mask), _DTYPES[q.dtype], _ptr(kv_lens),
@@ -249,7 +270,8 @@ def backward_deterministic_workspace_size(B: int, H: int, N: int) -> int:
 
 def backward(q, k, v, o, lse, do, *, causal: bool = False, scale: Optional[float] = None,
              block_mask=None, kv_lens=None, dq=None, dk=None, dv=None, workspace=None,
-             stream=None, deterministic: bool = False):
+             stream=None, deterministic: bool = False, dropout_p: float = 0.0, seed: int = 0,
+             offset: int = 0):
     """dQ, dK, dV = recompute-based attention backward (fa_backward; fa_backward_gqa when k, v
     have fewer heads than q; fa_backward_deterministic, bit-reproducible, when asked)."""
     B, H, N, d, Hkv = _check_qkv(q, k, v)
@@ -263,13 +285,22 @@ def backward(q, k, v, o, lse, do, *, causal: bool = False, scale: Optional[float
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    need = (backward_deterministic_workspace_size(B, H, N) if deterministic
+    need = (backward_deterministic_workspace_size(B, H, N) if deterministic or dropout_p > 0.0
             else backward_workspace_size(B, H, N, d))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv))
     tail = (d, scale, int(bool(causal)), _ptr(block_mask), _DTYPES[q.dtype], _ptr(kv_lens),
             _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if dropout_p > 0.0:
+        drop = FaDropout(float(dropout_p), int(seed), int(offset))
+        st = lib.fa_backward_dropout(*args, B, H, Hkv, N, d, scale, int(bool(causal)),
+                                     _ptr(block_mask), _DTYPES[q.dtype], _ptr(kv_lens),
+                                     ctypes.byref(drop), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream))
+        if st != FA_OK:
+            raise FaError(st, "fa_backward_dropout")
+        return dq, dk, dv
     if deterministic:
         st = lib.fa_backward_deterministic(*args, B, H, Hkv, N, *tail)
         if st != FA_OK:

@@ -104,15 +104,32 @@ struct Packing {
   int total;
 };
 
+// Host form of the dropout arguments (validated; disabled when nothing is dropped).
+fa_status make_dropout(const fa_dropout* in, fa::DropoutArgs* out) {
+  *out = fa::DropoutArgs{};
+  if (in == nullptr) return FA_ERR_INVALID_ARG;
+  if (!isfinite(in->p) || in->p < 0.f || in->p > 1.f) return FA_ERR_INVALID_ARG;
+  long long k8 = llrint((1.0 - (double)in->p) * 256.0);
+  k8 = k8 < 0 ? 0 : (k8 > 256 ? 256 : k8);
+  out->enabled = k8 < 256 ? 1 : 0;
+  out->seed_lo = (uint32_t)(in->seed & 0xFFFFFFFFull);
+  out->seed_hi = (uint32_t)(in->seed >> 32);
+  out->offset = in->offset;
+  out->k8 = (int)k8;
+  out->scale = k8 > 0 ? 256.f / (float)k8 : 0.f;
+  return FA_OK;
+}
+
 fa_status forward_impl(const void* q, const void* k, const void* v, void* o, float* lse,
                        int B, int H, int Hkv, int N, int d, float scale, int causal,
                        const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
-                       void* stream, Packing pk = {nullptr, 0}) {
+                       void* stream, Packing pk = {nullptr, 0}, fa::DropoutArgs drop = {}) {
   fa_status st = check_common(B, H, N, d, scale, dtype);
   if (st != FA_OK) return st;
   st = check_heads(H, Hkv, dtype);
   if (st != FA_OK) return st;
-  if (pk.cu_seqlens != nullptr && dtype == FA_FP32) return FA_ERR_UNSUPPORTED;
+  if ((pk.cu_seqlens != nullptr || drop.enabled) && dtype == FA_FP32) return FA_ERR_UNSUPPORTED;
+  if (pk.cu_seqlens != nullptr && drop.enabled) return FA_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0 || (pk.cu_seqlens != nullptr && pk.total == 0)) return FA_OK;
   if (block_mask != nullptr && N > kMaxBlockSparseN) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
@@ -130,6 +147,7 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
   a.cu_seqlens = pk.cu_seqlens;
   a.rows = pk.cu_seqlens != nullptr ? pk.total : N;
   if (pk.cu_seqlens != nullptr) a.heads_fastest = 1;     // sequences of unequal length
+  a.drop = drop;
   if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = dtype == FA_FP32 ? fa::launch_fwd_simt(a, dtype, s) : fa::launch_fwd_sm103(a, dtype, s);
@@ -236,16 +254,18 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
                         int B, int H, int Hkv, int N, int d, float scale, int causal,
                         const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
                         void* workspace, size_t workspace_bytes, void* stream,
-                        bool deterministic, Packing pk = {nullptr, 0}) {
+                        bool deterministic, Packing pk = {nullptr, 0}, fa::DropoutArgs drop = {}) {
   fa_status st = check_common(B, H, N, d, scale, dtype);
   if (st != FA_OK) return st;
   st = check_heads(H, Hkv, dtype);
   if (st != FA_OK) return st;
-  if ((deterministic || pk.cu_seqlens != nullptr) && dtype == FA_FP32) return FA_ERR_UNSUPPORTED;
+  if ((deterministic || pk.cu_seqlens != nullptr || drop.enabled) && dtype == FA_FP32)
+    return FA_ERR_UNSUPPORTED;
+  if (pk.cu_seqlens != nullptr && drop.enabled) return FA_ERR_UNSUPPORTED;
   // 16-bit inputs run the two-pass backward unless the fused one was selected (packed sequences
   // always take the two-pass one); fp32 always runs the CUDA-core backward (which adds dQ from
   // several blocks).
-  const bool two_pass = deterministic || pk.cu_seqlens != nullptr ||
+  const bool two_pass = deterministic || pk.cu_seqlens != nullptr || drop.enabled ||
                         (dtype != FA_FP32 && g_bwd_variant.load() == FA_BWD_TWO_PASS);
   // workspace sizes count the query rows of all slices: B*H*N, or H*total when packed
   const int wB = pk.cu_seqlens != nullptr ? 1 : B, wN = pk.cu_seqlens != nullptr ? pk.total : N;
@@ -280,6 +300,7 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
   a.cu_seqlens = pk.cu_seqlens;
   a.rows = pk.cu_seqlens != nullptr ? pk.total : N;
   if (pk.cu_seqlens != nullptr) a.heads_fastest = 1;     // sequences of unequal length
+  a.drop = drop;
   if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = fa::launch_bwd_preprocess(a, dtype, s);
@@ -324,6 +345,31 @@ fa_status fa_backward_deterministic(const void* q, const void* k, const void* v,
                                     size_t workspace_bytes, void* stream) {
   return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal, block_mask,
                        dtype, kv_lens, workspace, workspace_bytes, stream, true);
+}
+
+fa_status fa_forward_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int Hkv, int N, int d, float scale, int causal,
+                             const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                             const fa_dropout* dropout, void* stream) {
+  fa::DropoutArgs drop;
+  const fa_status st = make_dropout(dropout, &drop);
+  if (st != FA_OK) return st;
+  return forward_impl(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, block_mask, dtype, kv_lens,
+                      stream, Packing{nullptr, 0}, drop);
+}
+
+fa_status fa_backward_dropout(const void* q, const void* k, const void* v, const void* o,
+                              const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                              int B, int H, int Hkv, int N, int d, float scale, int causal,
+                              const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                              const fa_dropout* dropout, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  fa::DropoutArgs drop;
+  const fa_status st = make_dropout(dropout, &drop);
+  if (st != FA_OK) return st;
+  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal, block_mask,
+                       dtype, kv_lens, workspace, workspace_bytes, stream, true, Packing{nullptr, 0},
+                       drop);
 }
 
 fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,

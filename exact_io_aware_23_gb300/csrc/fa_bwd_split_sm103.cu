@@ -20,15 +20,18 @@ namespace {
 
 static_assert(dkdv::kThreads == dqp::kThreads, "both passes run with the same block size");
 
-template <int D, bool F16>
+// 320 threads = 10 warps, one CTA per SM.  The warps are spread over the SM's four 16K-register
+// partitions, three on some of them, so a thread may hold at most 16384 / 96 -> 168 registers
+// (a 200-register build does not launch).
+template <int D, bool F16, bool kDrop>
 __global__ void __launch_bounds__(dkdv::kThreads, 1)
 bwd_split_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const BwdArgs a, const int n_kv_units, const int n_q_units) {
   (void)n_q_units;
   const int x = (int)blockIdx.x;
-  if (x < n_kv_units) dkdv::run<D, F16>(x, tmQ, tmK, tmV, tmDO, a);
-  else dqp::run<D, F16>(x - n_kv_units, tmQ, tmK, tmV, tmDO, a);
+  if (x < n_kv_units) dkdv::run<D, F16, kDrop>(x, tmQ, tmK, tmV, tmDO, a);
+  else dqp::run<D, F16, kDrop>(x - n_kv_units, tmQ, tmK, tmV, tmDO, a);
 }
 
 cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH, bool f16) {
@@ -40,7 +43,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH, boo
                            3, base, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool kDrop>
 cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv, mdo;
   const int BH = a.B * a.H;            // query-side work units per tile row (Q, dO, dQ)
@@ -53,7 +56,7 @@ cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
   if ((e = make_map(&mk, a.k, D, a.rows, kv_slices, F16)) != cudaSuccess) return e;
   if ((e = make_map(&mv, a.v, D, a.rows, kv_slices, F16)) != cudaSuccess) return e;
   if ((e = make_map(&mdo, a.dO, D, a.rows, q_slices, F16)) != cudaSuccess) return e;
-  auto kern = bwd_split_sm103_kernel<D, F16>;
+  auto kern = bwd_split_sm103_kernel<D, F16, kDrop>;
   // each pass keeps its barriers 256 bytes below its live-tile bitmap (one bit per tile)
   const int bitmap = a.block_mask != nullptr ? ((a.n_tiles + 127) / 128) * 16 : 0;
   int smem = max(dkdv::Cfg<D, F16>::kSmem, dqp::Cfg<D, F16>::kSmem);
@@ -70,8 +73,12 @@ cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_bwd_split_sm103(const BwdArgs& a, fa_dtype dt, cudaStream_t s) {
-  if (dt == FA_FP16) return a.d == 64 ? launch<64, true>(a, s) : launch<128, true>(a, s);
-  return a.d == 64 ? launch<64, false>(a, s) : launch<128, false>(a, s);
+  if (a.drop.enabled) {
+    if (dt == FA_FP16) return a.d == 64 ? launch<64, true, true>(a, s) : launch<128, true, true>(a, s);
+    return a.d == 64 ? launch<64, false, true>(a, s) : launch<128, false, true>(a, s);
+  }
+  if (dt == FA_FP16) return a.d == 64 ? launch<64, true, false>(a, s) : launch<128, true, false>(a, s);
+  return a.d == 64 ? launch<64, false, false>(a, s) : launch<128, false, false>(a, s);
 }
 
 }  // namespace fa

@@ -31,6 +31,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include "dropout_sm103.cuh"
 #include "fa_internal.cuh"
 #include "fa_sm103.cuh"
 #include "ptx_sm103.cuh"
@@ -106,7 +107,7 @@ struct Geo {
   }
 };
 
-template <int D, bool F16>
+template <int D, bool F16, bool kDrop>
 __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                     const CUtensorMap& tmV, const CUtensorMap& tmDO,
                                     const BwdArgs& a) {
@@ -346,6 +347,10 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
     for (int hg = 0; hg < G && ok; ++hg)
     for (int i = g.next(g.i_begin); i < g.i_end; i = g.next(i + 1), ++n) {
       const int vs = n & 1;
+      // dropout: this key's keep bits over the warpgroup's 64 queries (generated while the
+      // scores are still being computed); the mask slice is that of query head hk*G + hg
+      uint64_t keep = ~0ull;
+      if constexpr (kDrop) keep = keep_col64(a.drop, (uint32_t)(b * a.H + hk * G + hg), i * BM + wg * 64, key);
       // the vectors of this tile were written before its Q copy was started
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full[n % C::kQSlots]), (uint32_t)(n / C::kQSlots) & 1u,
                           lim_ms, a.err);
@@ -385,7 +390,14 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
+        for (int e = 0; e < 32; ++e) {
+          if constexpr (kDrop) {                     // dV takes the dropped-out probabilities
+            const uint32_t kb = (uint32_t)(keep >> (2 * e)) & 3u;
+            pk[e] = ptx::pack2<F16>((kb & 1u) ? p[2 * e] : 0.f, (kb & 2u) ? p[2 * e + 1] : 0.f);
+          } else {
+            pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
+          }
+        }
         ptx::tmem_st32(tX, pk);
         ptx::tmem_wait_st();
       }
@@ -407,8 +419,12 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int col = hc * 32 + e;
-            const float2 dd = ptx::sub2(make_float2(__uint_as_float(raw[hc][e]), __uint_as_float(raw[hc][e + 1])),
-                                        *reinterpret_cast<const float2*>(dl + col));
+            float2 dpv = make_float2(__uint_as_float(raw[hc][e]), __uint_as_float(raw[hc][e + 1]));
+            if constexpr (kDrop) {                   // dP = (dO V^T) * M * 256/k8
+              const uint32_t kb = (uint32_t)(keep >> col) & 3u;
+              dpv = make_float2((kb & 1u) ? dpv.x * a.drop.scale : 0.f, (kb & 2u) ? dpv.y * a.drop.scale : 0.f);
+            }
+            const float2 dd = ptx::sub2(dpv, *reinterpret_cast<const float2*>(dl + col));
             const float2 ds = ptx::mul2(make_float2(p[col], p[col + 1]), dd);
             p[col] = ds.x;
             p[col + 1] = ds.y;
@@ -435,7 +451,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_done), 0, lim_ms, a.err);
       ptx::tc_fence_after();
     }
-    const float mult = wg == 0 ? 1.f : a.scale;
+    const float mult = wg == 0 ? (kDrop ? a.drop.scale : 1.f) : a.scale;
     uint16_t* out = static_cast<uint16_t*>(wg == 0 ? a.dv : a.dk) + ((size_t)ks * a.rows + row0 + key) * D;
     const uint32_t src = wg == 0 ? C::kDV : C::kDK;
 #pragma unroll 1

@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include "dropout_sm103.cuh"
 #include "fa_internal.cuh"
 #include "fa_sm103.cuh"
 #include "ptx_sm103.cuh"
@@ -104,7 +105,7 @@ struct Geo {
   }
 };
 
-template <int D, bool F16>
+template <int D, bool F16, bool kDrop>
 __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                     const CUtensorMap& tmV, const CUtensorMap& tmDO,
                                     const BwdArgs& a) {
@@ -317,6 +318,10 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
       const int kind = g.kind(j);
       const int k0 = j * BN + wg * 64;              // first key of this warpgroup's columns
       const uint32_t sb = C::kS + (uint32_t)(n & 1) * 128 + wg * 64;
+      // dropout: this row's keep bits over the warpgroup's 64 keys (generated while the scores
+      // are still being computed)
+      uint64_t keep = ~0ull;
+      if constexpr (kDrop) keep = keep_row64(a.drop, (uint32_t)bh, q, k0);
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[n & 1]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
       if (!ok) break;
       ptx::tc_fence_after();
@@ -359,8 +364,12 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int col = hc * 32 + e;
-            const float2 dpd = ptx::sub2(make_float2(__uint_as_float(raw[hc][e]), __uint_as_float(raw[hc][e + 1])),
-                                         dd2);
+            float2 dpv = make_float2(__uint_as_float(raw[hc][e]), __uint_as_float(raw[hc][e + 1]));
+            if constexpr (kDrop) {                   // dP = (dO V^T) * M * 256/k8
+              const uint32_t kb = (uint32_t)(keep >> col) & 3u;
+              dpv = make_float2((kb & 1u) ? dpv.x * a.drop.scale : 0.f, (kb & 2u) ? dpv.y * a.drop.scale : 0.f);
+            }
+            const float2 dpd = ptx::sub2(dpv, dd2);
             const float2 ds = ptx::mul2(make_float2(p[col], p[col + 1]), dpd);
             p[col] = ds.x;
             p[col + 1] = ds.y;

@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include "dropout_sm103.cuh"
 #include "fa_internal.cuh"
 #include "fa_sm103.cuh"
 #include "ptx_sm103.cuh"
@@ -106,7 +107,7 @@ struct Geo {
   }
 };
 
-template <int D, bool F16>
+template <int D, bool F16, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, FwdArgs a) {
@@ -334,6 +335,13 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     bool ok = true;
     int idx = 0;
     for (int j = g.next(g.j0); j < g.j_end; j = g.next(j + 1), ++idx) {
+      // dropout: this row's keep bits for the tile's 128 keys (generated while the scores are
+      // still being computed)
+      uint64_t keep[2] = {~0ull, ~0ull};
+      if constexpr (kDrop) {
+        keep[0] = keep_row64(a.drop, (uint32_t)g.bh, i, j * BN);
+        keep[1] = keep_row64(a.drop, (uint32_t)g.bh, i, j * BN + 64);
+      }
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[t]), idx & 1, lim_ms, a.err);
       if (!ok) break;
       ptx::tc_fence_after();
@@ -402,8 +410,13 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           for (int e = 0; e < 32; ++e) {
             const float2 x = ptx::fma2(make_float2(s[half * 64 + 2 * e], s[half * 64 + 2 * e + 1]), c2, nm2);
             const float2 pp = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
-            ls[e & 3] = ptx::add2(ls[e & 3], pp);
-            pk[e] = ptx::pack2<F16>(pp.x, pp.y);
+            ls[e & 3] = ptx::add2(ls[e & 3], pp);      // the normaliser counts every allowed key
+            if constexpr (kDrop) {
+              const uint32_t kb = (uint32_t)(keep[half] >> (2 * e)) & 3u;
+              pk[e] = ptx::pack2<F16>((kb & 1u) ? pp.x : 0.f, (kb & 2u) ? pp.y : 0.f);
+            } else {
+              pk[e] = ptx::pack2<F16>(pp.x, pp.y);
+            }
           }
           ptx::tmem_st32(tS + half * 32, pk);
         }
@@ -422,7 +435,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       ptx::tc_fence_after();
     }
     const bool any = l_run > 0.f;
-    const float inv = any ? 1.f / l_run : 0.f;
+    const float inv = any ? (kDrop ? a.drop.scale : 1.f) / l_run : 0.f;
     const size_t row = (size_t)g.qs * a.rows + g.row0 + i;      // this query row on its axis
     uint16_t* orow = static_cast<uint16_t*>(a.o) + row * D;
     // split-KV: this range's normalised partial output (fp32) and log-sum-exp
@@ -482,7 +495,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH, boo
                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool kDrop>
 cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
   // token axis and slice count of the tensor maps: per (b, h) slice, or packed per head
@@ -492,7 +505,7 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   if ((e = make_map(&mq, a.q, D, a.rows, q_slices, F16)) != cudaSuccess) return e;
   if ((e = make_map(&mk, a.k, D, packed ? a.rows : a.Nk, kv_slices, F16)) != cudaSuccess) return e;
   if ((e = make_map(&mv, a.v, D, packed ? a.rows : a.Nk, kv_slices, F16)) != cudaSuccess) return e;
-  auto kern = fwd_sm103_kernel<D, F16>;
+  auto kern = fwd_sm103_kernel<D, F16, kDrop>;
   // + the live-tile bitmap of a block-sparse mask (one bit per key tile)
   const int smem = Cfg<D, F16>::kSmem + (a.block_mask != nullptr ? ((a.n_tiles + 127) / 128) * 16 : 0);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -510,8 +523,12 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_fwd_sm103(const FwdArgs& a, fa_dtype dt, cudaStream_t s) {
-  if (dt == FA_FP16) return a.d == 64 ? launch<64, true>(a, s) : launch<128, true>(a, s);
-  return a.d == 64 ? launch<64, false>(a, s) : launch<128, false>(a, s);
+  if (a.drop.enabled) {
+    if (dt == FA_FP16) return a.d == 64 ? launch<64, true, true>(a, s) : launch<128, true, true>(a, s);
+    return a.d == 64 ? launch<64, false, true>(a, s) : launch<128, false, true>(a, s);
+  }
+  if (dt == FA_FP16) return a.d == 64 ? launch<64, true, false>(a, s) : launch<128, true, false>(a, s);
+  return a.d == 64 ? launch<64, false, false>(a, s) : launch<128, false, false>(a, s);
 }
 
 }  // namespace fa

@@ -19,6 +19,16 @@ struct DebugKnobs {
   uint32_t wait_limit_ms;  // bound of every mbarrier wait
 };
 
+// Dropout on P (see dropout_sm103.cuh for the generator and the mask layout).  Zero-initialised
+// arguments mean no dropout.
+struct DropoutArgs {
+  int enabled;
+  uint32_t seed_lo, seed_hi;   // Philox key
+  uint32_t offset;             // Philox counter word 3
+  int k8;                      // keep iff the element's 8-bit uniform is below k8 (0..256)
+  float scale;                 // 256 / k8, or 0 when k8 == 0
+};
+
 struct FwdArgs {
   const void* q;
   const void* k;
@@ -48,6 +58,7 @@ struct FwdArgs {
   // sequence and Q, K, V, O are [H or Hkv, rows, d].  Without them rows = N.
   const int32_t* cu_seqlens;
   int rows;
+  DropoutArgs drop;
 };
 
 struct SplitMergeArgs {       // combines the split-KV partials with the (m, l, u) merge law
@@ -84,6 +95,7 @@ struct BwdArgs {
   int heads_fastest;          // launch order: (b, h) slice fastest (unequal work per tile)
   const int32_t* cu_seqlens;  // packed sequences, as in FwdArgs
   int rows;
+  DropoutArgs drop;
 };
 
 // Rows of the query-side tensors (Q, O, dO, dQ, LSE, D) over all slices.

@@ -118,6 +118,35 @@ fa_status fa_backward_deterministic(const void* q, const void* k, const void* v,
                                     size_t workspace_bytes, void* stream);
 
 /*
+ * Dropout on the attention probabilities (the "dropout RNG" of the pages' list of production
+ * semantics, replayed in the backward).  Element (i, j) of slice (b, h) is kept with probability
+ * k8 / 256, k8 = round((1 - p) * 256), and kept probabilities are scaled by 256 / k8:
+ *     O = (P * M * 256/k8) V,  LSE as without dropout.
+ * M is regenerated, never stored: Philox4x32-10 (Salmon et al., SC 2011) with key = seed and
+ * counter (j / 4, i / 4, b*H + h, offset); byte (j mod 4) of output word (i mod 4) is the
+ * element's 8-bit uniform, kept iff below k8.  The backward with the same seed and offset
+ * replays the same mask.  p must lie in [0, 1]; p = 0 is plain attention.
+ */
+typedef struct {
+  float p;          /* dropout probability */
+  uint64_t seed;    /* generator key */
+  uint32_t offset;  /* counter word 3: distinct offsets give independent masks for one seed */
+} fa_dropout;
+
+/* fa_forward_gqa with dropout (bf16/fp16; no packed sequences, no split-KV). */
+fa_status fa_forward_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int Hkv, int N, int d, float scale, int causal,
+                             const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                             const fa_dropout* dropout, void* stream);
+/* The matching backward (two-pass; workspace fa_backward_deterministic_workspace_size(B, H, N)). */
+fa_status fa_backward_dropout(const void* q, const void* k, const void* v, const void* o,
+                              const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                              int B, int H, int Hkv, int N, int d, float scale, int causal,
+                              const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                              const fa_dropout* dropout, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
  * Packed sequences ("ragged offsets" and the "document mask" in the pages' list of production
  * semantics, "FlashAttention：让精确注意力服从内存层次", list after the CPU reference).  n_seqs
  * sequences of different lengths are stored back to back along each head's token axis:

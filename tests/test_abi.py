@@ -207,3 +207,29 @@ def test_varlen_argument_checks(lib):
         assert call(S=0, cu=None) == OK
     assert fwd_v(d=80) == UNSUPPORTED
     assert bwd_v(wsb=ws - 4) == INVALID
+
+
+def test_dropout_argument_checks(lib):
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+    class Drop(ctypes.Structure):
+        _fields_ = [("p", ctypes.c_float), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint32)]
+    dp = ctypes.POINTER(Drop)
+    lib.fa_forward_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, dp, vp]
+    lib.fa_backward_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i,
+                                        vp, dp, vp, sz, vp]
+    assert ctypes.sizeof(Drop) == 24          # float, 64-bit seed (8-aligned), 32-bit offset
+
+    def fwd_d(p=0.1, drop=True, dtype=0, N=128):
+        d = ctypes.byref(Drop(p, 1, 0)) if drop else None
+        return lib.fa_forward_dropout(P, P, P, P, P, 1, 2, 2, N, 64, 0.125, 0, None, dtype, None, d, None)
+
+    def bwd_d(p=0.1, dtype=0, N=100):
+        return lib.fa_backward_dropout(P, P, P, P, P, P, P, P, P, 1, 2, 2, N, 64, 0.125, 0, None, dtype,
+                                       None, ctypes.byref(Drop(p, 1, 0)), P, 1 << 20, None)
+    for bad in (float("nan"), -0.1, 1.5, float("inf")):
+        assert fwd_d(p=bad) == INVALID and bwd_d(p=bad) == INVALID
+    assert fwd_d(drop=False) == INVALID
+    assert fwd_d(dtype=1) == UNSUPPORTED and bwd_d(dtype=1) == UNSUPPORTED
+    assert fwd_d(N=0) == OK and bwd_d(N=0) == OK
+    assert fwd_d(p=0.0, dtype=1, N=0) == OK    # no dropout: plain attention rules apply
