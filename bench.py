@@ -212,6 +212,8 @@ def run_ours(args, w):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa.backward_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
     kw = dict(causal=w.causal, scale=w.scale, block_mask=bm, kv_lens=kl)
+    if args.dropout > 0.0:
+        kw.update(dropout_p=args.dropout, seed=1234, offset=0)
     bkw = dict(kw, deterministic=args.deterministic)
 
     def step():
@@ -298,7 +300,8 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": dict(workload_config(w),
-                       backward="fused_atomic_dq" if args.fused_backward else "two_pass"),
+                       backward="fused_atomic_dq" if args.fused_backward else "two_pass",
+                       **({"dropout": args.dropout} if args.dropout > 0.0 else {})),
         "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
         "fwd_bwd_tflops_algorithmic": world * 3.5 * F / (ms_step * 1e-3) / 1e12,
         "pct_of_bf16_peak": {"forward": fwd_tf / peak, "fwd_bwd": value / world / peak,
@@ -404,6 +407,62 @@ def run_decode(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_varlen(args, w):
+    """Packed-sequence workloads: one step = fa_forward_varlen + fa_backward_varlen over all the
+    packed sequences; FLOPs summed per sequence (4*H*L^2*d, halved when causal)."""
+    import torch
+
+    import exact_io_aware_23_gb300 as fa
+    from workloads import make_packed_inputs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    x = make_packed_inputs(w, seed=0)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    cu, maxl = x["cu_seqlens"].to(dev), x["max_seqlen"]
+    H, T, d = q.shape
+    kw = dict(causal=w.causal, scale=w.scale)
+
+    def fwd():
+        return fa.forward_varlen(q, k, v, cu, maxl, **kw)
+
+    o, lse = fwd()
+    for _ in range(args.warmup):
+        o, lse = fwd()
+        fa.backward_varlen(q, k, v, o, lse, do, cu, maxl, **kw)
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(0) as clocks:
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            o, lse = fwd()
+            ev[i][1].record(stream)
+            fa.backward_varlen(q, k, v, o, lse, do, cu, maxl, **kw)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    if fa.check_device_status() != 0:
+        raise RuntimeError("device error during the timed region")
+    t_fwd = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    t_bwd = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    F = sum(4.0 * H * n * n * d for n in w.seq_lens) * (0.5 if w.causal else 1.0)
+    ms = t_fwd + t_bwd
+    peaks, src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    bwd_tf = 2.5 * F / (t_bwd * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": 2.5 * F / (ms * 1e-3) / 1e12, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": dict(workload_config(w), n_seqs=len(w.seq_lens), max_seqlen=maxl, total=T),
+            "fwd_tflops": F / (t_fwd * 1e-3) / 1e12, "bwd_tflops": bwd_tf,
+            "ms_fwd": t_fwd, "ms_bwd": t_bwd,
+            "roofline": {"bound": "tensor", "kernel": "fa_backward_varlen (all launches of the call)",
+                         "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
+                         "traffic": None, "peak_source": f"bf16_tflops of {src}"},
+            "gpu_launches": 3 * args.steps, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -416,6 +475,8 @@ def main():
                     help="call fa_backward_deterministic (the default two-pass backward, by name)")
     ap.add_argument("--fused-backward", action="store_true",
                     help="time the fused atomic-dQ backward variant (fa_set_backward_variant)")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="dropout probability on P for the timed forward and backward")
     ap.add_argument("--cpu-rows", type=int, default=16384)
     ap.add_argument("--ref-rows", type=int, default=1024)
     args = ap.parse_args()
@@ -425,6 +486,8 @@ def main():
         run_reference(args, w)
     elif w.Nk is not None:
         run_decode(args, w)
+    elif w.seq_lens is not None:
+        run_varlen(args, w)
     else:
         run_ours(args, w)
 

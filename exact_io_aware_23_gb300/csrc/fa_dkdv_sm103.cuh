@@ -68,6 +68,7 @@ struct Bars {             // at most 256 bytes (the live-tile bitmap follows)
   uint64_t q_empty[4];
   uint64_t o_full[4];
   uint64_t o_empty[4];
+  uint64_t vec_full[2];
   uint64_t vec_empty[2];
   uint64_t s_full;
   uint64_t dp_full;
@@ -165,6 +166,8 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
       ptx::mbar_init(ptx::smem_u32(&bars->o_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->o_empty[s]), 1);
     }
+    ptx::mbar_init(ptx::smem_u32(&bars->vec_full[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->vec_full[1]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->vec_empty[0]), 8);
     ptx::mbar_init(ptx::smem_u32(&bars->vec_empty[1]), 8);
     ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
@@ -209,6 +212,9 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
           ptx::tma_load_3d(sbase + C::kV + hh * 128 * 128, &tmV, kb, hh * 64, row0 + g.k0, ks);
         }
       }
+      // Per tile: start the Q and dO copies first, then fetch the tile's vectors (plain loads,
+      // whose latency then overlaps the copies').  nq / no count the copies started, for the drain.
+      int nq = 0, no = 0;
       for (int hg = 0; hg < G && ok; ++hg)
       for (int i = g.next(g.i_begin); i < g.i_end && ok; i = g.next(i + 1), ++n) {
         const int bhq = bhq0 + hg;
@@ -216,8 +222,24 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
         if (lane == 0) {
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_empty[qs]), ((uint32_t)(n / C::kQSlots) & 1u) ^ 1u,
                               lim_ms, a.err);
-          if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->vec_empty[vs]), ((uint32_t)(n >> 1) & 1u) ^ 1u,
-                                      lim_ms, a.err);
+          if (ok) {
+            const uint32_t qb = ptx::smem_u32(&bars->q_full[qs]);
+            ptx::mbar_arrive_expect_tx(qb, C::kTile);
+            for (int hh = 0; hh < D / 64; ++hh)
+              ptx::tma_load_3d(sbase + C::kQ + qs * C::kTile + hh * 128 * 128, &tmQ, qb, hh * 64, row0 + i * BM, bhq);
+            ++nq;
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->o_empty[os]), ((uint32_t)(n / C::kOSlots) & 1u) ^ 1u,
+                                lim_ms, a.err);
+          }
+          if (ok) {
+            const uint32_t ob = ptx::smem_u32(&bars->o_full[os]);
+            ptx::mbar_arrive_expect_tx(ob, C::kTile);
+            for (int hh = 0; hh < D / 64; ++hh)
+              ptx::tma_load_3d(sbase + C::kO + os * C::kTile + hh * 128 * 128, &tmDO, ob, hh * 64, row0 + i * BM, bhq);
+            ++no;
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->vec_empty[vs]), ((uint32_t)(n >> 1) & 1u) ^ 1u,
+                                lim_ms, a.err);
+          }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -232,29 +254,14 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
           dl[r] = q < g.N ? a.delta[row] : 0.f;
         }
         __syncwarp();
-        if (lane == 0) {
-          const uint32_t qb = ptx::smem_u32(&bars->q_full[qs]);
-          ptx::mbar_arrive_expect_tx(qb, C::kTile);
-          for (int hh = 0; hh < D / 64; ++hh)
-            ptx::tma_load_3d(sbase + C::kQ + qs * C::kTile + hh * 128 * 128, &tmQ, qb, hh * 64, row0 + i * BM, bhq);
-          ok = ptx::mbar_wait(ptx::smem_u32(&bars->o_empty[os]), ((uint32_t)(n / C::kOSlots) & 1u) ^ 1u,
-                              lim_ms, a.err);
-          if (ok) {
-            const uint32_t ob = ptx::smem_u32(&bars->o_full[os]);
-            ptx::mbar_arrive_expect_tx(ob, C::kTile);
-            for (int hh = 0; hh < D / 64; ++hh)
-              ptx::tma_load_3d(sbase + C::kO + os * C::kTile + hh * 128 * 128, &tmDO, ob, hh * 64, row0 + i * BM, bhq);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) { ++n; break; }
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->vec_full[vs]));
       }
       if (lane == 0) {   // drain: copies in flight must land before shared memory is released
         ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, lim_ms, a.err);
-        for (int m = max(0, n - C::kQSlots); m < n; ++m)
+        for (int m = max(0, nq - C::kQSlots); m < nq; ++m)
           ptx::mbar_wait(ptx::smem_u32(&bars->q_full[m % C::kQSlots]), (uint32_t)(m / C::kQSlots) & 1u,
                          lim_ms, a.err);
-        for (int m = max(0, n - C::kOSlots); m < n; ++m)
+        for (int m = max(0, no - C::kOSlots); m < no; ++m)
           ptx::mbar_wait(ptx::smem_u32(&bars->o_full[m % C::kOSlots]), (uint32_t)(m / C::kOSlots) & 1u,
                          lim_ms, a.err);
       }
@@ -350,10 +357,8 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
       // dropout: this key's keep bits over the warpgroup's 64 queries (generated while the
       // scores are still being computed); the mask slice is that of query head hk*G + hg
       uint64_t keep = ~0ull;
-      if constexpr (kDrop) keep = keep_col64(a.drop, (uint32_t)(b * a.H + hk * G + hg), i * BM + wg * 64, key);
-      // the vectors of this tile were written before its Q copy was started
-      ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full[n % C::kQSlots]), (uint32_t)(n / C::kQSlots) & 1u,
-                          lim_ms, a.err);
+      if constexpr (kDrop) keep = keep_col64_own(a.drop, (uint32_t)(b * a.H + hk * G + hg), i * BM + wg * 64, key);
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->vec_full[vs]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
       if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full), (uint32_t)n & 1u, lim_ms, a.err);
       if (!ok) break;
       ptx::tc_fence_after();

@@ -321,7 +321,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
       // dropout: this row's keep bits over the warpgroup's 64 keys (generated while the scores
       // are still being computed)
       uint64_t keep = ~0ull;
-      if constexpr (kDrop) keep = keep_row64(a.drop, (uint32_t)bh, q, k0);
+      if constexpr (kDrop) keep = keep_row64_own(a.drop, (uint32_t)bh, q, k0);
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[n & 1]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
       if (!ok) break;
       ptx::tc_fence_after();

@@ -35,11 +35,20 @@ class Workload:
     backward: bool = True
     Nk: Optional[int] = None          # key length when it differs from N (decode shapes)
     Hkv: Optional[int] = None         # key/value heads when fewer than H (grouped-query attention)
+    seq_lens: Optional[tuple] = None  # packed sequences: their lengths (B = 1, N = their sum)
 
     @property
     def scale(self) -> float:
         return 1.0 / float(self.d) ** 0.5
 
+
+def packed_lengths(n: int, lo: int, hi: int, seed: int) -> tuple:
+    """n sequence lengths ~ U{lo..hi} from a seeded CPU generator (input structure only)."""
+    g = torch.Generator().manual_seed(seed)
+    return tuple(int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g))
+
+
+_VARLEN = packed_lengths(24, 256, 4096, seed=7)
 
 WORKLOADS = {
     # fp32 correctness case: B1 H1 N128 d64, non-causal, forward only
@@ -62,6 +71,9 @@ WORKLOADS = {
     # grouped-query attention: 32 query heads on 8 key/value heads, B2 N8192 d128, causal
     "gqa_causal_n8k_h32_kv8_d128": Workload("gqa_causal_n8k_h32_kv8_d128", 2, 32, 8192, 128,
                                             "bf16", causal=True, Hkv=8),
+    # packed sequences: 24 sequences of U{256..4096} tokens back to back, H16 d128, causal
+    "varlen_causal_h16_d128": Workload("varlen_causal_h16_d128", 1, 16, sum(_VARLEN), 128, "bf16",
+                                       causal=True, seq_lens=_VARLEN),
     # block-sparse attention B1 H8 N65536 d64, local band + global tiles
     "block_sparse_n64k_d64": Workload("block_sparse_n64k_d64", 1, 8, 65536, 64, "bf16",
                                       block_sparse=True),
@@ -129,3 +141,16 @@ def random_tile_mask(n_tiles: int, density: float, seed: int) -> torch.Tensor:
 def as_f64(t: torch.Tensor):
     """The exact values of a (possibly bf16) tensor as a float64 numpy array."""
     return t.to(torch.float64).numpy()
+
+
+def make_packed_inputs(w: Workload, seed: int = 0) -> dict:
+    """Inputs of a packed-sequence workload: q, k, v, dO as [heads, total, d] (same recipe and
+    draw order as ``make_inputs``), the int32 offsets [n_seqs + 1] and the longest length."""
+    x = make_inputs(w, seed=seed)
+    offs = [0]
+    for n in w.seq_lens:
+        offs.append(offs[-1] + n)
+    out = {n: x[n][0] for n in ("q", "k", "v", "do")}
+    out.update(cu_seqlens=torch.tensor(offs, dtype=torch.int32), max_seqlen=max(w.seq_lens),
+               causal=w.causal, scale=w.scale, dtype=w.dtype)
+    return out
