@@ -347,11 +347,12 @@ def run_decode(args, w):
     dev = torch.device("cuda", 0)
     x = make_inputs(w, seed=0)
     B, H, Nq, d = x["q"].shape
-    Nk = x["k"].shape[2]
+    Nk, Hkv = x["k"].shape[2], x["k"].shape[1]
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
-    splits = int(fa.lib.fa_forward_splitkv_auto_splits(B, H, Nq, Nk))
+    # grouped heads: a group's G * Nq queries run as one block against its key/value head
+    splits = int(fa.lib.fa_forward_splitkv_auto_splits(B, Hkv, (H // Hkv) * Nq, Nk))
     ws = torch.empty(int(fa.lib.fa_forward_splitkv_workspace_size(B, H, Nq, d, splits)), dtype=torch.uint8, device=dev)
     step = lambda: fa.forward_splitkv(q, k, v, scale=w.scale, n_splits=splits, o=o, lse=lse, workspace=ws)
     for _ in range(args.warmup):
@@ -389,7 +390,7 @@ def run_decode(args, w):
     e2e_ms = e0.elapsed_time(e1) / args.steps
     F = 4.0 * B * H * Nq * Nk * d
     elt = q.element_size()
-    algo_bytes = elt * (2 * B * H * Nk * d + 2 * B * H * Nq * d) + 4 * B * H * Nq
+    algo_bytes = elt * (2 * B * Hkv * Nk * d + 2 * B * H * Nq * d) + 4 * B * H * Nq
     peaks, src = load_peaks()
     gbs = algo_bytes / (ms * 1e-3) / 1e9
     line = {"metric": METRIC, "value": F / (ms * 1e-3) / 1e12, "unit": UNIT, "n_gpus": 1,

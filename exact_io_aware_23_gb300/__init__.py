@@ -81,6 +81,8 @@ def _load() -> ctypes.CDLL:
     L.fa_set_backward_variant.argtypes = [i]
     L.fa_set_backward_variant.restype = i
     L.fa_forward_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, i, vp, sz, vp]
+    L.fa_forward_splitkv_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, i, i, vp, sz, vp]
+    L.fa_forward_splitkv_gqa.restype = i
     L.fa_forward_splitkv.restype = i
     L.fa_forward_splitkv_workspace_size.argtypes = [i, i, i, i, i]
     L.fa_forward_splitkv_workspace_size.restype = sz
@@ -232,29 +234,38 @@ def forward_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *,
                     n_splits: int = 0, o: Optional[torch.Tensor] = None,
                     lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """O, LSE with the key sequence cut into ranges merged afterwards (fa_forward_splitkv).
-    q: [B, H, Nq, d]; k, v: [B, H, Nk, d]; bf16 or fp16; no causal or tile mask."""
+    """O, LSE with the key sequence cut into ranges merged afterwards (fa_forward_splitkv;
+    fa_forward_splitkv_gqa when k, v have fewer heads).  q: [B, H, Nq, d]; k, v: [B, Hkv, Nk, d]
+    with Hkv dividing H; bf16 or fp16; no causal or tile mask."""
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
             raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
     B, H, Nq, d = q.shape
-    Nk = k.shape[2]
-    if k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != d:
-        raise ValueError("k, v must be [B, H, Nk, d] matching q")
+    Nk, Hkv = k.shape[2], k.shape[1]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d or H % Hkv != 0:
+        raise ValueError("k, v must be [B, Hkv, Nk, d] with Hkv dividing the query heads")
     if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DTYPES:
         raise ValueError("q, k, v must share a supported dtype")
     scale = 1.0 / d ** 0.5 if scale is None else float(scale)
     _, kv_lens = _masks(None, kv_lens, B, Nq, q.device)
-    splits = int(lib.fa_forward_splitkv_auto_splits(B, H, Nq, Nk)) if n_splits == 0 else int(n_splits)
+    G = H // Hkv                       # a group's query heads run as one block of G * Nq rows
+    splits = (int(lib.fa_forward_splitkv_auto_splits(B, Hkv, G * Nq, Nk)) if n_splits == 0
+              else int(n_splits))
     splits = max(1, min(splits, (Nk + 127) // 128 or 1))
     need = int(lib.fa_forward_splitkv_workspace_size(B, H, Nq, d, splits))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
-    st = lib.fa_forward_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
-                                scale, _ptr(kv_lens), _DTYPES[q.dtype], splits, _ptr(workspace),
-                                workspace.numel() * workspace.element_size(), _stream(stream))
+    if Hkv == H:
+        st = lib.fa_forward_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                                    scale, _ptr(kv_lens), _DTYPES[q.dtype], splits, _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream))
+    else:
+        st = lib.fa_forward_splitkv_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Nq,
+                                        Nk, d, scale, _ptr(kv_lens), _DTYPES[q.dtype], splits,
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream))
     if st != FA_OK:
         raise FaError(st, "fa_forward_splitkv")
     return o, lse

@@ -347,6 +347,22 @@ fa_status fa_backward_deterministic(const void* q, const void* k, const void* v,
                        dtype, kv_lens, workspace, workspace_bytes, stream, true);
 }
 
+fa_status fa_forward_splitkv_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
+                                 const int32_t* kv_lens, fa_dtype dtype, int n_splits,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || H < 0 || Nq < 0) return FA_ERR_INVALID_ARG;
+  const fa_status st = check_heads(H, Hkv, dtype);
+  if (st != FA_OK) return st;
+  if (B == 0 || H == 0 || Nq == 0) return fa_forward_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale,
+                                                             kv_lens, dtype, n_splits, workspace,
+                                                             workspace_bytes, stream);
+  const long long rows = (long long)(H / Hkv) * Nq;     // a group's queries, contiguous
+  if (rows > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  return fa_forward_splitkv(q, k, v, o, lse, B, Hkv, (int)rows, Nk, d, scale, kv_lens, dtype,
+                            n_splits, workspace, workspace_bytes, stream);
+}
+
 fa_status fa_forward_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
                              int B, int H, int Hkv, int N, int d, float scale, int causal,
                              const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,

@@ -193,6 +193,21 @@ fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* 
                              const int32_t* kv_lens, fa_dtype dtype, int n_splits,
                              void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * fa_forward_splitkv for grouped-query attention (decode with H query heads on Hkv key/value
+ * heads; k, v are [B, Hkv, Nk, d]).  The G = H / Hkv query heads of a group are consecutive in
+ * [B, H, Nq, d], so their G * Nq queries form one block of rows that is attended against the
+ * group's key/value head in one pass: each K/V tile is read once per group instead of once per
+ * query head, and short query blocks fill the 128-row tiles.  Equivalent to
+ * fa_forward_splitkv(q, k, v, o, lse, B, Hkv, G * Nq, Nk, ...); n_splits = 0 therefore uses
+ * fa_forward_splitkv_auto_splits(B, Hkv, G * Nq, Nk), and the workspace is
+ * fa_forward_splitkv_workspace_size(B, H, Nq, d, n_splits) (the same number of rows).
+ */
+fa_status fa_forward_splitkv_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
+                                 const int32_t* kv_lens, fa_dtype dtype, int n_splits,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
 /* Workspace bytes of fa_forward_splitkv (fp32 partial O and LSE of every range). */
 size_t fa_forward_splitkv_workspace_size(int B, int H, int Nq, int d, int n_splits);
 

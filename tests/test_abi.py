@@ -233,3 +233,20 @@ def test_dropout_argument_checks(lib):
     assert fwd_d(dtype=1) == UNSUPPORTED and bwd_d(dtype=1) == UNSUPPORTED
     assert fwd_d(N=0) == OK and bwd_d(N=0) == OK
     assert fwd_d(p=0.0, dtype=1, N=0) == OK    # no dropout: plain attention rules apply
+
+
+def test_splitkv_gqa_argument_checks(lib):
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_forward_splitkv_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, i, i, vp, sz, vp]
+    lib.fa_forward_splitkv_workspace_size.argtypes = [i, i, i, i, i]
+    lib.fa_forward_splitkv_workspace_size.restype = sz
+    ws = lib.fa_forward_splitkv_workspace_size(2, 8, 16, 128, 4)
+
+    def call(H=8, Hkv=2, Nq=16, dtype=0, wsb=ws):
+        return lib.fa_forward_splitkv_gqa(P, P, P, P, P, 2, H, Hkv, Nq, 4096, 128, 0.1, None, dtype, 4,
+                                          P, wsb, None)
+    assert call(Hkv=3) == UNSUPPORTED
+    assert call(Hkv=0) == INVALID
+    assert call(dtype=1) == UNSUPPORTED
+    assert call(wsb=ws - 256) == INVALID          # same workspace as the ungrouped call
+    assert call(Nq=0) == OK

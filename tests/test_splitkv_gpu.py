@@ -81,3 +81,28 @@ def test_decode_workload():
                           heads=[0, 9])
     assert_bf16_close("O", f64(o)[:, [0, 9]][:, :, rows], O)
     assert_lse_close(f64(lse)[:, [0, 9]][:, :, rows], L, LSE_TOL)
+
+
+@pytest.mark.parametrize("H,Hkv", [(8, 1), (8, 2), (32, 8)])
+@pytest.mark.parametrize("Nq,Nk", [(1, 3000), (16, 4096), (5, 777)])
+def test_splitkv_grouped_heads(H, Hkv, Nq, Nk):
+    """Grouped-query decode: the G query heads of a group run as one block of G * Nq rows against
+    their shared key/value head; every query head still gets its own softmax."""
+    w = Workload("dec_gqa", 2, H, Nq, 128, "bf16", Nk=Nk, backward=False)
+    x = make_inputs(w, seed=H + Nq + Nk, kv_heads=Hkv)
+    x["kv_lens"] = torch.tensor([Nk, Nk // 3 + 1], dtype=torch.int32)
+    for n_splits in (0, 3):
+        o, lse = _run(x, n_splits)
+        _check(x, o, lse)
+
+
+def test_splitkv_grouped_equals_repeated_heads():
+    """Same numbers as the ungrouped split-KV forward on key/value heads repeated per query head
+    (within rounding: the packed row block changes which rows share a tile, not the arithmetic
+    of a row)."""
+    w = Workload("dec_gqa", 2, 8, 16, 128, "bf16", Nk=5000, backward=False)
+    x = make_inputs(w, seed=4, kv_heads=2)
+    o1, l1 = _run(x, 4)
+    xr = dict(x, k=x["k"].repeat_interleave(4, dim=1), v=x["v"].repeat_interleave(4, dim=1))
+    o2, l2 = _run(xr, 4)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)

@@ -74,6 +74,10 @@ WORKLOADS = {
     # packed sequences: 24 sequences of U{256..4096} tokens back to back, H16 d128, causal
     "varlen_causal_h16_d128": Workload("varlen_causal_h16_d128", 1, 16, sum(_VARLEN), 128, "bf16",
                                        causal=True, seq_lens=_VARLEN),
+    # grouped-query decode: 32 query heads on 8 key/value heads, 16 new queries per sequence
+    # against a 32K-key cache (forward only)
+    "decode_gqa_q16_k32k_h32_kv8_d128": Workload("decode_gqa_q16_k32k_h32_kv8_d128", 8, 32, 16, 128,
+                                                 "bf16", backward=False, Nk=32768, Hkv=8),
     # block-sparse attention B1 H8 N65536 d64, local band + global tiles
     "block_sparse_n64k_d64": Workload("block_sparse_n64k_d64", 1, 8, 65536, 64, "bf16",
                                       block_sparse=True),
