@@ -47,12 +47,17 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# host-only translation units (argument checks, descriptor encoding): not part of the kernels
+HOST_ONLY_SOURCES = {"fa_api.cu", "fa_noalloc.cu", "fa_tmap.cu"}
+
+
 def kernel_source_hash():
+    """Hash of the device-code sources (a traffic record stays valid while they are unchanged)."""
     h = hashlib.sha256()
     for d in KERNEL_SOURCES:
         base = os.path.join(ROOT, d)
         for fn in sorted(os.listdir(base)):
-            if fn.endswith((".cu", ".cuh")):
+            if fn.endswith((".cu", ".cuh")) and fn not in HOST_ONLY_SOURCES:
                 with open(os.path.join(base, fn), "rb") as f:
                     h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
