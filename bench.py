@@ -357,7 +357,8 @@ def run_decode(args, w):
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
     # grouped heads: a group's G * Nq queries run as one block against its key/value head
-    splits = int(fa.lib.fa_forward_splitkv_auto_splits(B, Hkv, (H // Hkv) * Nq, Nk))
+    splits = (args.splits if args.splits > 0
+              else int(fa.lib.fa_forward_splitkv_auto_splits(B, Hkv, (H // Hkv) * Nq, Nk)))
     ws = torch.empty(int(fa.lib.fa_forward_splitkv_workspace_size(B, H, Nq, d, splits)), dtype=torch.uint8, device=dev)
     step = lambda: fa.forward_splitkv(q, k, v, scale=w.scale, n_splits=splits, o=o, lse=lse, workspace=ws)
     for _ in range(args.warmup):
@@ -483,6 +484,8 @@ def main():
                     help="time the fused atomic-dQ backward variant (fa_set_backward_variant)")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="dropout probability on P for the timed forward and backward")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="key ranges of the split-KV decode workloads (0: the library's choice)")
     ap.add_argument("--cpu-rows", type=int, default=16384)
     ap.add_argument("--ref-rows", type=int, default=1024)
     args = ap.parse_args()

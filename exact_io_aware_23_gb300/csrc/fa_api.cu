@@ -184,7 +184,19 @@ int fa_forward_splitkv_auto_splits(int B, int H, int Nq, int Nk) {
   want = want < 1 ? 1 : want;
   const long long cap = (kv_tiles + 1) / 2 < 64 ? (kv_tiles + 1) / 2 : 64;   // >= 2 tiles each
   if (want > cap) want = cap < 1 ? 1 : cap;
-  return (int)want;
+  // From there, the fewest ranges whose CTAs fill their last wave of one-CTA-per-SM launches to
+  // at least 95 % (a ragged last wave left most of the SMs idle at the end: on a 32K-key decode
+  // the best count measured 1.1-1.3x faster than the first count above it); else the fullest
+  // last wave among up to four times as many ranges.
+  long long best = want;
+  double best_fill = 0.0;
+  for (long long s = want; s <= cap && s <= 4 * want; ++s) {
+    const long long ctas = units * s, waves = (ctas + sms - 1) / sms;
+    const double fill = (double)ctas / (double)(waves * sms);
+    if (fill >= 0.95) return (int)s;
+    if (fill > best_fill + 1e-9) { best_fill = fill; best = s; }
+  }
+  return (int)best;
 }
 
 size_t fa_forward_splitkv_workspace_size(int B, int H, int Nq, int d, int n_splits) {

@@ -211,8 +211,9 @@ fa_status fa_forward_splitkv_gqa(const void* q, const void* k, const void* v, vo
 /* Workspace bytes of fa_forward_splitkv (fp32 partial O and LSE of every range). */
 size_t fa_forward_splitkv_workspace_size(int B, int H, int Nq, int d, int n_splits);
 
-/* The number of ranges fa_forward_splitkv uses for n_splits = 0: about two CTAs per SM of the
- * current device, at least two key tiles per range, at most 64 ranges. */
+/* The number of ranges fa_forward_splitkv uses for n_splits = 0: at least about two CTAs per SM
+ * of the current device, then the fewest ranges whose CTAs fill their last wave (one CTA per SM)
+ * to 95 %; at least two key tiles per range, at most 64 ranges. */
 int fa_forward_splitkv_auto_splits(int B, int H, int Nq, int Nk);
 
 /* Bytes of workspace fa_backward needs for these sizes (a multiple of 256). */
