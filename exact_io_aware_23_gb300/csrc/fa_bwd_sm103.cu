@@ -211,11 +211,19 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         // -LSE (as a log2-domain bias; -inf where P must vanish) and D for the tile's rows
         float* lse2 = reinterpret_cast<float*>(smem + C::kVec + st * 1024);
         float* dl = lse2 + 128;
-        for (int r = lane; r < 128; r += 32) {
-          const int q = i * BM + r;
-          float L = q < a.N ? a.lse[(size_t)bhq * a.N + q] : -INFINITY;
-          lse2[r] = L == -INFINITY ? -INFINITY : -L * kLog2e;   // stored negated
-          dl[r] = q < a.N ? a.delta[(size_t)bhq * a.N + q] : 0.f;
+        // all eight loads of a lane first, then the stores (which could alias the loads as far
+        // as the compiler knows)
+        float Lv[4], Dv[4];
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int q = i * BM + lane + 32 * k4;
+          Lv[k4] = q < a.N ? __ldg(a.lse + (size_t)bhq * a.N + q) : -INFINITY;
+          Dv[k4] = q < a.N ? __ldg(a.delta + (size_t)bhq * a.N + q) : 0.f;
+        }
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          lse2[lane + 32 * k4] = Lv[k4] == -INFINITY ? -INFINITY : -Lv[k4] * kLog2e;   // negated
+          dl[lane + 32 * k4] = Dv[k4];
         }
         __syncwarp();
         if (lane == 0) {

@@ -246,12 +246,20 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
         // -LSE as a log2-domain bias (-inf where P must vanish) and D for the tile's rows
         float* lse2 = reinterpret_cast<float*>(smem + C::kVec + vs * 1024);
         float* dl = lse2 + 128;
-        for (int r = lane; r < 128; r += 32) {
-          const int q = i * BM + r;
+        // all eight loads of a lane first (the stores below could alias them as far as the
+        // compiler knows, which would otherwise serialise four round trips to memory)
+        float Lv[4], Dv[4];
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int q = i * BM + lane + 32 * k4;
           const size_t row = (size_t)bhq * a.rows + row0 + q;
-          const float L = q < g.N ? a.lse[row] : -INFINITY;
-          lse2[r] = L == -INFINITY ? -INFINITY : -L * kLog2e;
-          dl[r] = q < g.N ? a.delta[row] : 0.f;
+          Lv[k4] = q < g.N ? __ldg(a.lse + row) : -INFINITY;
+          Dv[k4] = q < g.N ? __ldg(a.delta + row) : 0.f;
+        }
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          lse2[lane + 32 * k4] = Lv[k4] == -INFINITY ? -INFINITY : -Lv[k4] * kLog2e;
+          dl[lane + 32 * k4] = Dv[k4];
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->vec_full[vs]));
