@@ -7,9 +7,10 @@
 // LSE = m + ln l are written once at the end.
 //
 // GB300 design (one CTA = two 128-row Q tiles of one (b, h) slice, 384 threads):
-//   warp 8      TMA producer: Q tiles once, then K_j, V_j for every live key tile j through a
-//               ring of shared-memory slots (mbarrier full/empty pairs).  Masked tiles are never
-//               loaded ("FlashAttention paper story", block-sparse paragraph).
+//   warp 8      TMA producer: Q tiles once, then K_j for every live key tile j through a ring of
+//               shared-memory slots (mbarrier full/empty pairs).  Masked tiles are never loaded
+//               ("FlashAttention paper story", block-sparse paragraph).
+//   warp 10     TMA producer of V_j, through a ring of its own.
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T (SS MMA, 128 x 128 x d) into TMEM, and
 //               O_t += P_t V_j (TS MMA: P_t read from TMEM, V_j from shared memory).
 //   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1: each thread owns one query row
@@ -46,7 +47,9 @@ enum : int { kNone = 0, kPartial = 1, kFull = 2 };
 template <int D, bool F16>
 struct Cfg {
   static constexpr int kTileBytes = BN * D * 2;                 // one K or V tile; one Q tile
-  static constexpr int kSlots = D == 128 ? 5 : 8;               // K/V ring depth
+  static constexpr int kSlots = D == 128 ? 5 : 8;               // K and V slots in all
+  static constexpr int kKSlots = D == 128 ? 3 : 4;              // K ring: slots [0, kKSlots)
+  static constexpr int kVSlots = kSlots - kKSlots;              // V ring: the rest
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
@@ -224,42 +227,54 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       for (int t = 0; t < 2; ++t)
         for (int hh = 0; hh < D / 64; ++hh)
           ptx::tma_load_3d(sQ + t * C::kTileBytes + hh * BM * 128, &tmQ, qbar, hh * 64, g.row0 + g.q0 + t * BM, g.qs);
-      int n = 0;
+      int n = 0;                                   // K tiles issued
       bool ok = true;
-      for (int j = g.next(g.j0); j < g.j_end && ok; j = g.next(j + 1)) {
-        for (int kind = 0; kind < 2 && ok; ++kind, ++n) {
-          const int slot = n % C::kSlots;
-          const uint32_t ph = (n / C::kSlots) & 1;
-          ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[slot]), ph ^ 1, lim_ms, a.err);
-          if (!ok) break;
-          if (a.dbg.inject == 1 && n == 0) continue;      // test hook: never deliver this tile
-          const uint32_t fb = ptx::smem_u32(&bars->kv_full[slot]);
-          ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
-          const CUtensorMap* m = kind == 0 ? &tmK : &tmV;
-          for (int hh = 0; hh < D / 64; ++hh)
-            ptx::tma_load_3d(sKV + slot * C::kTileBytes + hh * BN * 128, m, fb, hh * 64, g.row0 + j * BN, g.ks);
-        }
+      for (int j = g.next(g.j0); j < g.j_end && ok; j = g.next(j + 1), ++n) {
+        const int slot = n % C::kKSlots;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[slot]), ((n / C::kKSlots) & 1) ^ 1, lim_ms, a.err);
+        if (!ok) break;
+        if (a.dbg.inject == 1 && n == 0) continue;      // test hook: never deliver this tile
+        const uint32_t fb = ptx::smem_u32(&bars->kv_full[slot]);
+        ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
+        for (int hh = 0; hh < D / 64; ++hh)
+          ptx::tma_load_3d(sKV + slot * C::kTileBytes + hh * BN * 128, &tmK, fb, hh * 64, g.row0 + j * BN, g.ks);
       }
-      // Drain: every copy this CTA issued must have landed before shared memory is released.
+      // Drain: every copy this thread issued must have landed before shared memory is released.
       ptx::mbar_wait(qbar, 0, lim_ms, a.err);
-      for (int m = max(0, n - C::kSlots); m < n; ++m) {
+      for (int m = max(0, n - C::kKSlots); m < n; ++m) {
         if (a.dbg.inject == 1 && m == 0) continue;
-        ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[m % C::kSlots]), (m / C::kSlots) & 1, lim_ms, a.err);
+        ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[m % C::kKSlots]), (m / C::kKSlots) & 1, lim_ms, a.err);
       }
+    } else if (warp == 10 && lane == 0) {
+      // ------------------------------- TMA producer of V ------------------------------------
+      // K and V have rings of their own, each with its own producer thread, so a K tile (freed
+      // as soon as both S products have read it) is refilled without queueing behind a V slot
+      // (freed only after both PV products of the next key tile).
+      int n = 0;                                   // V tiles issued
+      bool ok = true;
+      for (int j = g.next(g.j0); j < g.j_end && ok; j = g.next(j + 1), ++n) {
+        const int slot = C::kKSlots + n % C::kVSlots;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[slot]), ((n / C::kVSlots) & 1) ^ 1, lim_ms, a.err);
+        if (!ok) break;
+        const uint32_t fb = ptx::smem_u32(&bars->kv_full[slot]);
+        ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
+        for (int hh = 0; hh < D / 64; ++hh)
+          ptx::tma_load_3d(sKV + slot * C::kTileBytes + hh * BN * 128, &tmV, fb, hh * 64, g.row0 + j * BN, g.ks);
+      }
+      for (int m = max(0, n - C::kVSlots); m < n; ++m)
+        ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[C::kKSlots + m % C::kVSlots]), (m / C::kVSlots) & 1, lim_ms, a.err);
     } else if (warp == 9 && lane == 0) {
       // ------------------------------- MMA issuer ---------------------------------------------
       bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, lim_ms, a.err);
       ptx::tc_fence_after();
-      int n = 0, idx = 0;
+      int idx = 0;
       int prev_v = -1;
       uint32_t prev_vph = 0;
       for (int j = g.next(g.j0); j < g.j_end && ok; j = g.next(j + 1), ++idx) {
-        const int kslot = n % C::kSlots;
-        const uint32_t kph = (n / C::kSlots) & 1;
-        ++n;
-        const int vslot = n % C::kSlots;
-        const uint32_t vph = (n / C::kSlots) & 1;
-        ++n;
+        const int kslot = idx % C::kKSlots;
+        const uint32_t kph = (idx / C::kKSlots) & 1;
+        const int vslot = C::kKSlots + idx % C::kVSlots;
+        const uint32_t vph = (idx / C::kVSlots) & 1;
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[kslot]), kph, lim_ms, a.err);
         if (ok && idx > 0) ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[prev_v]), prev_vph, lim_ms, a.err);
         if (!ok) break;
