@@ -332,7 +332,9 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
           if (!ok) break;
           ptx::tc_fence_after();
           acc_mma(C::kDK, C::kY, sbase + C::kQ + qs * C::kTile, n == 0);
-          ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qs]));
+          // no commit frees Q_n: dP^T(n+1), issued next, comes after both products that read it,
+          // so the compute warps free it on seeing dP^T(n+1) (a commit stalls the tensor pipe
+          // for about as long as one MMA)
           if (more) {                                 // dP^T(n+1) into Y, behind dK(n)
             ok = ptx::mbar_wait(ptx::smem_u32(&bars->o_full[os1]), (uint32_t)((n + 1) / C::kOSlots) & 1u,
                                 lim_ms, a.err);
@@ -420,6 +422,9 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->dp_full), (uint32_t)n & 1u, lim_ms, a.err);
       if (!ok) break;
       ptx::tc_fence_after();
+      // dP^T(n) has completed, and with it dK(n-1), the last product to read Q_{n-1}
+      if (n > 0 && warp == 0 && lane == 0)
+        ptx::mbar_arrive(ptx::smem_u32(&bars->q_empty[(n - 1) % C::kQSlots]));
       // dS^T = P^T * (dP^T - D)
       {
         uint32_t raw[2][32];

@@ -269,9 +269,10 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
             if (!ok) break;
             ptx::tc_fence_after();
             dq_mma(n - 1);
-            ptx::mma_commit(ptx::smem_u32(&bars->k_empty[(n - 1) % C::kKSlots]));
           }
-          // dP(n) = dO V_j^T; V_j is free once this product is done
+          // dP(n) = dO V_j^T.  No commit frees V_j or K_{j-1}: dP(n) is issued after every product
+          // that reads them, so the compute warps, on seeing dP(n), free both (a commit stalls
+          // the tensor pipe for about as long as one MMA).
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_full[vslot]), (uint32_t)(n / C::kVSlots) & 1u,
                               lim_ms, a.err);
           if (!ok) break;
@@ -284,14 +285,12 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
                         ptx::sdesc_sw128(sv + off, 16, 1024), C::kIdescS, kk > 0);
           }
           ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
-          ptx::mma_commit(ptx::smem_u32(&bars->v_empty[vslot]));
         }
         if (ok && n > 0) {
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_ready), (uint32_t)(n - 1) & 1u, lim_ms, a.err);
           if (ok) {
             ptx::tc_fence_after();
             dq_mma(n - 1);
-            ptx::mma_commit(ptx::smem_u32(&bars->k_empty[(n - 1) % C::kKSlots]));
           }
         }
       }
@@ -353,6 +352,12 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->dp_full), (uint32_t)n & 1u, lim_ms, a.err);
       if (!ok) break;
       ptx::tc_fence_after();
+      if (warp == 0 && lane == 0) {
+        // dP(n) has completed, and with it every MMA issued before it: V_j is free, and so is
+        // K_{j-1} (its dQ product came before dP(n))
+        ptx::mbar_arrive(ptx::smem_u32(&bars->v_empty[n % C::kVSlots]));
+        if (n > 0) ptx::mbar_arrive(ptx::smem_u32(&bars->k_empty[(n - 1) % C::kKSlots]));
+      }
       {
         uint32_t raw[2][32];
 #pragma unroll

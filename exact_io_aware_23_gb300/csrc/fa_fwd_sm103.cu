@@ -292,7 +292,6 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               ptx::mma_ts(tmem + 256 + t * D, tmem + t * BN + kk * 8, bdesc, C::kIdescO,
                           (idx > 1 || kk > 0) ? 1u : 0u);
             }
-            if (t == 1) ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[prev_v]));
           }
           // S_t = Q_t K_j^T
           const uint32_t qbase = sQ + t * C::kTileBytes;
@@ -306,7 +305,9 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           }
           ptx::mma_commit(ptx::smem_u32(&bars->s_full[t]));
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[kslot]));
+        // No commit frees K_j or V_{j-1}: S_1(j) is issued after every product that reads them,
+        // so the softmax of Q tile 1, on seeing S_1(j), frees both (a commit stalls the tensor
+        // pipe for about as long as one MMA).
         prev_v = vslot;
         prev_vph = vph;
       }
@@ -326,7 +327,6 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           }
           ptx::mma_commit(ptx::smem_u32(&bars->pv_done[t]));
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[prev_v]));
       }
       // every MMA this thread issued has finished before TMEM and shared memory are released
       ptx::mma_commit(ptx::smem_u32(&bars->mma_done));
@@ -360,6 +360,12 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[t]), idx & 1, lim_ms, a.err);
       if (!ok) break;
       ptx::tc_fence_after();
+      if (t == 1 && sub == 0 && lane == 0) {
+        // S_1(j) has completed, and with it every MMA issued before it: both S products of key
+        // tile j (K_j's slot is free) and both PV products of the previous tile (V's slot too).
+        ptx::mbar_arrive(ptx::smem_u32(&bars->kv_empty[idx % C::kKSlots]));
+        if (idx > 0) ptx::mbar_arrive(ptx::smem_u32(&bars->kv_empty[C::kKSlots + (idx - 1) % C::kVSlots]));
+      }
       const int kind = g.kind(t, j);
       uint32_t pk[32];
       if (kind == kNone) {
