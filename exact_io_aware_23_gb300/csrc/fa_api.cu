@@ -176,7 +176,7 @@ fa_status fa_forward_gqa(const void* q, const void* k, const void* v, void* o, f
 
 int fa_forward_splitkv_auto_splits(int B, int H, int Nq, int Nk) {
   if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return 1;
-  int dev = 0, sms = 148;
+  int dev = 0, sms = 152;                   // GB300's SM count when no device can be asked
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long units = (long long)B * H * ((Nq + 255) / 256);   // CTAs without splitting
   const int kv_tiles = (Nk + 127) / 128;

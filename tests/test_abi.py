@@ -124,6 +124,41 @@ def test_splitkv_argument_checks(lib):
     assert call(Nq=0) == OK
 
 
+def test_splitkv_auto_splits_fill_the_last_wave(lib):
+    """The split count rule, on the host (no device: the rule assumes GB300's 152 SMs): from about
+    two CTAs per SM, the fewest ranges whose CTAs fill their last one-CTA-per-SM wave to 95 %,
+    capped at 2 key tiles a range and at 64 ranges."""
+    lib.fa_forward_splitkv_auto_splits.argtypes = [ctypes.c_int] * 4
+    auto = lib.fa_forward_splitkv_auto_splits
+    sms = 152
+
+    def rule(B, H, Nq, Nk):                       # the rule restated, to compare against
+        units = B * H * -(-Nq // 256)
+        tiles = -(-Nk // 128)
+        want = max(1, -(-2 * sms // units))
+        cap = min((tiles + 1) // 2, 64)
+        want = min(want, max(cap, 1))
+        best, best_fill = want, 0.0
+        for s in range(want, min(cap, 4 * want) + 1):
+            ctas = units * s
+            fill = ctas / (-(-ctas // sms) * sms)
+            if fill >= 0.95:
+                return s
+            if fill > best_fill + 1e-9:
+                best, best_fill = s, fill
+        return best
+
+    # the two decode workloads: 128 and 64 query blocks against 32K keys -> 7 ranges each
+    assert auto(8, 16, 16, 32768) == 7
+    assert auto(8, 8, 64, 32768) == 7
+    for B, H, Nq, Nk in [(1, 1, 16, 512), (1, 1, 1, 1000000), (2, 3, 300, 4096), (4, 32, 16, 8192),
+                         (1, 8, 4096, 65536), (16, 16, 16, 128), (3, 5, 700, 20000)]:
+        got = auto(B, H, Nq, Nk)
+        assert got == rule(B, H, Nq, Nk), (B, H, Nq, Nk)
+        assert 1 <= got <= max(1, min(64, (-(-Nk // 128) + 1) // 2))
+    assert auto(0, 1, 1, 1) == 1 and auto(1, 1, 1, 0) == 1
+
+
 def test_gqa_argument_checks(lib):
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.fa_forward_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, vp]
