@@ -32,3 +32,20 @@ def test_value_scale_and_fp32():
     assert 1.3 < float(g["q"].float().std()) < 1.7 and g["causal"]
     f = make_inputs(WORKLOADS["fp32_n128_d64"])
     assert f["q"].dtype == torch.float32 and tuple(f["q"].shape) == (1, 1, 128, 64)
+
+
+def test_forward_flop_convention():
+    """The metric's FLOP count (4*B*H*N^2*d for the forward; half when causal; the kept share of
+    tiles when block-sparse), checked against the figures the workload table states."""
+    import bench
+    c4 = WORKLOADS["long_n16k_d128"]
+    assert abs(bench.forward_flops(c4, 1, 16, 16384) - 2199.02e9) < 0.01e9
+    c4c = WORKLOADS["long_n16k_d128_causal"]
+    assert bench.forward_flops(c4c, 1, 16, 16384) == bench.forward_flops(c4, 1, 16, 16384) / 2
+    c3 = WORKLOADS["gpt2_small_causal_n1024"]
+    assert abs(bench.forward_flops(c3, 8, 12, 1024) - 12.885e9) < 0.001e9
+    c5 = WORKLOADS["block_sparse_n64k_d64"]
+    bm = local_global_tile_mask(512)
+    got = bench.forward_flops(c5, 1, 8, 65536, block_mask=bm)
+    assert abs(got - 4.0 * 8 * 65536 ** 2 * 64 * 6614 / 512 ** 2) < 1.0
+    assert abs(got - 221.9e9) < 0.1e9
