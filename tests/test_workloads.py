@@ -49,3 +49,18 @@ def test_forward_flop_convention():
     got = bench.forward_flops(c5, 1, 8, 65536, block_mask=bm)
     assert abs(got - 4.0 * 8 * 65536 ** 2 * 64 * 6614 / 512 ** 2) < 1.0
     assert abs(got - 221.9e9) < 0.1e9
+
+
+def test_clock_summary_reads_reasons():
+    """The bench's clock record: median SM clock under load, the maximum, and which throttle
+    reasons were active in any sample (the fields nvidia-smi prints, in the order queried)."""
+    import bench
+    cs = bench.ClockSampler(0)
+    cs.rows = [["2070", "2070", "300.5", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"],
+               ["2055", "2070", "950.1", "0x4", "Not Active", "Not Active", "Not Active", "Active"],
+               ["2040", "2070", "1380.0", "0x4", "Not Active", "Not Active", "Not Active", "Active"]]
+    sm = cs.summary()
+    assert sm["sm_mhz"] == 2055.0 and sm["sm_max_mhz"] == 2070.0
+    assert sm["reasons"] == ["sw_power_cap"] and sm["power_w_max"] == 1380.0 and sm["samples"] == 3
+    cs.rows = []
+    assert cs.summary()["reasons"] == ["nvidia-smi unavailable"]
