@@ -32,7 +32,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_two_gloo_ranks():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:    # no fork of this multi-threaded process
         out = m.dict()
         mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
         res = dict(out)
