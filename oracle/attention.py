@@ -6,40 +6,40 @@ no code, constant or helper with the CUDA library.
 
 What it computes, and where the pages fix it:
 
-* Attention is ``softmax(QK^T / sqrt(d)) V`` (FlashAttention page 3, opening formula).  The
-  method "computes the same function as standard attention" (page 2, "Why the word 'exact' is
-  in the title"), so the oracle is that standard function, materialised: S = scale*Q K^T,
-  P = softmax(S) row by row, O = P V (page 3, "前序瓶颈" three-line listing).  ``scale`` is an
-  argument (page 1's pseudocode has none, page 3 uses 1/sqrt(d)).
-* Masks (page 3, list after the CPU reference: causal / padding masks "for production
-  semantics"; page 1, block-sparse paragraph: a tile mask says which blocks are computed).
+* Attention is ``softmax(QK^T / sqrt(d)) V`` ("FlashAttention：让精确注意力服从内存层次", opening formula).  The method "computes the same function as standard attention"
+  ("FlashAttention: Exact Attention with Less GPU Memory", "Why the word 'exact' is in the title"), so the oracle is that standard function, materialised: S = scale*Q K^T,
+  P = softmax(S) row by row, O = P V ("前序瓶颈" three-line listing of the same page).  ``scale`` is an
+  argument ("FlashAttention paper story"'s pseudocode has none, "FlashAttention：让精确注意力服从内存层次" uses 1/sqrt(d)).
+* Masks ("FlashAttention：让精确注意力服从内存层次", list after the "CPU reference": causal / padding masks for production
+  semantics; "FlashAttention paper story", block-sparse paragraph: a tile mask says which blocks are computed).
   Entry (i, j) of one (b, h) slice is allowed iff
   ``(not causal or j <= i) and j < kv_len[b] and block_mask[i // 128][j // 128] != 0``.
   Disallowed scores are -inf.  A row with no allowed key has O = 0 and LSE = -inf (the pages
-  only ask that fully masked rows be covered, page 3 "数值与正确性").
-* Statistics kept for the backward: page 1 (backward paragraph) keeps two length-N vectors
+  only ask that fully masked rows be covered, "FlashAttention：让精确注意力服从内存层次", "数值与正确性").
+* Statistics kept for the backward: "FlashAttention paper story" (backward paragraph) keeps two length-N vectors
   (running max and normaliser).  The oracle returns the one equivalent vector
   ``LSE_i = ln sum_j exp(s_ij)`` (natural log), computed stably as ``m_i + ln sum exp(s_ij - m_i)``.
-* Backward: the pages say only that P is recomputed from the stored statistics (page 1,
-  backward paragraph; page 2, "Tiling, and paying arithmetic to avoid memory").  The gradients
+* Backward: the pages say only that P is recomputed from the stored statistics ("FlashAttention paper story",
+  backward paragraph; "FlashAttention: Exact Attention with Less GPU Memory", "Tiling, and paying arithmetic to avoid memory").  The gradients
   of O = softmax(S) V with S = scale*Q K^T follow from the chain rule:
   dV = P^T dO;  dP = dO V^T;  D_i = sum_j P_ij dP_ij;  dS = P * (dP - D);
   dQ = scale * dS K;  dK = scale * dS^T Q.
   The oracle forms D from P and dP (its definition); the CUDA path uses rowsum(dO * O), equal
   in exact arithmetic.
-* ``online_attention`` and ``merge_stats`` restate the pages' own blockwise algorithm (page 1,
-  tiling and online softmax with a running max and running sum; page 3, "Online softmax" and the
-  (m, l, u) merge law) so that the dense oracle can be checked against the pages' claim that the
-  two agree (page 3, "CPU reference": error below 1e-12 on its worked example).
+* ``stats``, ``merge_stats`` and ``online_attention`` restate the pages' blockwise method: per
+  key group statistics (m, l, u) and their merge law ("FlashAttention：让精确注意力服从内存层次", "Online softmax"), folded over
+  the groups in key order (the running maximum and sum of "FlashAttention paper story", tiling and online
+  softmax), so that the dense oracle can be checked against the pages' claim that the two agree
+  ("FlashAttention：让精确注意力服从内存层次", "CPU reference": error below 1e-12 on its worked example).
 
-* Grouped-query attention (page 3, list after the CPU reference: "GQA head mapping" among the
+* Grouped-query attention ("FlashAttention：让精确注意力服从内存层次", list after the "CPU reference": "GQA head mapping" among the
   production semantics).  The pages name the feature only; the oracle takes the usual reading:
   with H query heads and Hkv key/value heads (Hkv dividing H), query head h attends with
   key/value head h // (H / Hkv), so consecutive query heads share one key/value head.  In the
   backward, dK and dV of a key/value head are the sums over the query heads that read it (the
   chain rule through the shared operand).
 
-* Ragged offsets and document masks (page 3, same list: "document mask" and "ragged offsets").
+* Ragged offsets and document masks (same page, same list: "document mask" and "ragged offsets").
   The pages name them only.  Reading: several sequences (documents) of lengths L_0, L_1, ...
   are packed back to back along the token axis, described by offsets ``segments`` =
   [0, L_0, L_0+L_1, ..., total]; a query attends only to keys of its own sequence (the
@@ -272,7 +272,7 @@ def backward(q, k, v, do, scale: float, causal: bool = False, kv_lens=None, bloc
 # --- the pages' own blockwise algorithm, for pinning the dense oracle -----------------------
 
 def stats(scores: np.ndarray, values: np.ndarray):
-    """(m, l, u) of one group of scores for one query (page 3, "Online softmax" statistics).
+    """(m, l, u) of one group of scores for one query ("FlashAttention：让精确注意力服从内存层次", "Online softmax").
 
     m = max_i s_i, l = sum_i exp(s_i - m), u = sum_i exp(s_i - m) v_i.  An empty or fully
     masked group is the identity (-inf, 0, 0).
@@ -287,7 +287,7 @@ def stats(scores: np.ndarray, values: np.ndarray):
 
 
 def merge_stats(a, b):
-    """Stable merge of two (m, l, u) triples (page 3, merge law under "Online softmax")."""
+    """Stable merge of two (m, l, u) triples ("FlashAttention：让精确注意力服从内存层次", merge law under "Online softmax")."""
     ma, la, ua = a
     mb, lb, ub = b
     m = max(ma, mb)
@@ -299,28 +299,30 @@ def merge_stats(a, b):
 
 
 def online_attention(q, k, v, scale: float, block_size: int):
-    """Blockwise attention with a running max and running normaliser (no masks).
+    """Blockwise attention for one (b, h) slice, no masks, built on the merge law.
 
-    For one (b, h) slice: q [Nq, d], k [Nk, d], v [Nk, dv].  Keys and values are visited one
-    block at a time; each query keeps its running maximum, normaliser and un-normalised output,
-    rescaling the old contributions by exp(m_old - m_new) whenever the maximum grows, and
-    divides by the normaliser at the end (page 1, tiling and online softmax; page 3, CPU
-    reference).  Returns (O [Nq, dv], LSE [Nq]).
+    q [Nq, d], k [Nk, d], v [Nk, dv].  The keys are cut into consecutive groups of
+    ``block_size``.  For every query, each group is reduced to its statistics (m, l, u) by
+    ``stats`` and the groups are combined, in key order, by ``merge_stats``; the result is
+    O = u / l and LSE = m + ln l ("FlashAttention：让精确注意力服从内存层次", section
+    "Online softmax": a tile's (m, l, u) can be computed on its own and merged; the same idea
+    as the running maximum and normaliser of "FlashAttention paper story", tiling and
+    online-softmax paragraphs).  A pure-Python loop over queries and groups: small inputs only.
+    Returns (O [Nq, dv], LSE [Nq]).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
-    nq = q.shape[0]
-    run_max = np.full(nq, -np.inf)
-    run_sum = np.zeros(nq)
-    acc = np.zeros((nq, v.shape[1]))
-    for start in range(0, k.shape[0], block_size):
-        kb, vb = k[start:start + block_size], v[start:start + block_size]
-        s = scale * (q @ kb.T)
-        new_max = np.maximum(run_max, s.max(axis=1))
-        shrink = np.exp(run_max - new_max)          # exp(-inf) = 0 on the first block
-        w = np.exp(s - new_max[:, None])
-        run_sum = shrink * run_sum + w.sum(axis=1)
-        acc = shrink[:, None] * acc + w @ vb
-        run_max = new_max
-    return acc / run_sum[:, None], run_max + np.log(run_sum)
+    groups = [np.arange(g0, min(g0 + block_size, k.shape[0]))
+              for g0 in range(0, k.shape[0], block_size)]
+    out = np.zeros((q.shape[0], v.shape[1]))
+    lse = np.full(q.shape[0], -np.inf)
+    for i, qi in enumerate(q):
+        total = (-math.inf, 0.0, np.zeros(v.shape[1]))
+        for cols in groups:
+            total = merge_stats(total, stats(scale * (k[cols] @ qi), v[cols]))
+        m, l, u = total
+        if l > 0.0:
+            out[i] = u / l
+            lse[i] = m + math.log(l)
+    return out, lse

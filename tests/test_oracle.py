@@ -26,16 +26,16 @@ def _one(x):
     return np.asarray(x, dtype=np.float64)[None, None]
 
 
-# --- page 3 worked example ------------------------------------------------------------------
+# --- worked example of the "CPU reference" section ------------------------------------------------------------------
 
 def _worked():
-    with open(os.path.join(GOLDEN, "worked_example_p3.json")) as f:
+    with open(os.path.join(GOLDEN, "worked_example_cpu_reference.json")) as f:
         g = json.load(f)
     return np.array(g["q"]), np.array(g["k"]), np.array(g["v"]), g
 
 
 def test_worked_example_blockwise_equals_dense():
-    """Page 3, "CPU reference": the blockwise result equals the dense one to < 1e-12 and is finite."""
+    """"FlashAttention：让精确注意力服从内存层次", "CPU reference": the blockwise result equals the dense one to < 1e-12 and is finite."""
     q, k, v, g = _worked()
     scale = 1.0 / math.sqrt(q.shape[1])
     O_dense, L_dense = oracle.forward(_one(q), _one(k), _one(v), scale)
@@ -46,7 +46,7 @@ def test_worked_example_blockwise_equals_dense():
 
 
 def test_worked_example_hand_scores():
-    """Brute force on the page 3 example with dot products worked out by hand.
+    """Brute force on the "CPU reference" example with dot products worked out by hand.
 
     q0 . k_j = [0, -1/2, 3, 3/2, -5/4] and q1 . k_j = [1, 9/2, 0, -2, 5/2]; the scores are these
     over sqrt(3).  LSE is the natural log of the sum of exponentials; O the weighted mean of v.
@@ -63,7 +63,7 @@ def test_worked_example_hand_scores():
             assert abs(O[0, 0, i, c] - expect) < 1e-13
 
 
-# --- merge law (page 3, "Online softmax") ---------------------------------------------------
+# --- merge law ("Online softmax") ---------------------------------------------------
 
 def _random_partition(n, rng):
     cuts = sorted(rng.choice(np.arange(1, n), size=rng.integers(1, min(n - 1, 8) + 1), replace=False))
@@ -124,7 +124,7 @@ def test_merge_matches_dense_output():
 
 @pytest.mark.parametrize("block", [1, 2, 3, 16, 64, 200])
 def test_online_algorithm_equals_dense(block):
-    """Page 1 / page 3: the running-max blockwise algorithm gives the dense result."""
+    """The blockwise algorithm (merge law folded over key groups) gives the dense result."""
     q, k, v = _rand((9, 5), 4, 2.0), _rand((57, 5), 5, 2.0), _rand((57, 2), 6)
     O, L = oracle.forward(_one(q), _one(k), _one(v), 0.7)
     Ob, Lb = oracle.online_attention(q, k, v, 0.7, block)

@@ -1,7 +1,7 @@
 """Plant plausible mistakes in a copy of the oracle (on the CPU) and check that the pins in
 test_oracle.py catch every one: a dropped scale, a sign, a transposed operand, an off-by-one in
-each mask, the wrong logarithm base, a wrong reduction axis, a wrong rescale direction in the
-pages' online algorithm, a wrong factor in the pages' merge law a wrong query-to-key/value
+each mask, the wrong logarithm base, a wrong reduction axis, a key group dropped in the
+blockwise algorithm, a wrong factor in the pages' merge law a wrong query-to-key/value
 head mapping and a sequence boundary off by one."""
 import os
 import shutil
@@ -25,7 +25,8 @@ MUTATIONS = [
     ("lse = m0 + np.log(np.exp(s - m0[:, None]).sum(axis=1))",
      "lse = m0 + np.log2(np.exp(s - m0[:, None]).sum(axis=1))"),
     ("O[b, hi, c0:c0 + r.size] = p @ v[b, g, cols]", "O[b, hi, c0:c0 + r.size] = p @ v[b, g, cols[::-1]]"),
-    ("shrink = np.exp(run_max - new_max)", "shrink = np.exp(new_max - run_max)"),
+    ("groups = [np.arange(g0, min(g0 + block_size, k.shape[0]))",
+     "groups = [np.arange(g0, min(g0 + block_size - 1, k.shape[0]))"),
     ("D = (do[b, h, r] * np.asarray(o, dtype=np.float64)[b, h, r]).sum(axis=1)",
      "D = (q[b, h, r] * np.asarray(o, dtype=np.float64)[b, h, r]).sum(axis=1)"),
     ("return m, fa * la + fb * lb, fa * np.asarray(ua) + fb * np.asarray(ub)",

@@ -81,7 +81,7 @@ def test_bf16_mask_combination():
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_bf16_extreme_logits(d):
-    """Scores pushed to about +-60 (page 3 asks for extreme logits to be covered)."""
+    """Scores pushed to about +-60 ("FlashAttention：让精确注意力服从内存层次", "数值与正确性", asks for extreme logits to be covered)."""
     x = _case(400, d, "bf16", False, B=1, H=2, seed=9)
     s = (x["q"].float() @ x["k"].float().transpose(-1, -2)).abs().max().item()
     x["scale"] = 60.0 / s

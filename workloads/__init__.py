@@ -5,8 +5,9 @@ the tile-sparsity pattern).  It holds none of the attention arithmetic, so the C
 and the CUDA path can both take their inputs from here without sharing any of the method.
 
 The workloads stand in for the ones the FlashAttention pages measure on (BERT-large at
-sequence 512, GPT-2 small at 1024, long-range 16K, block-sparse Path-256 at 64K; page 1,
-"results" table; page 2, "What it measured").  No dataset is used: values are i.i.d.
+sequence 512, GPT-2 small at 1024, long-range 16K, block-sparse Path-256 at 64K; "FlashAttention
+paper story", results table; "FlashAttention: Exact Attention with Less GPU Memory", "What it
+measured").  No dataset is used: values are i.i.d.
 normal, drawn in float32 from a CPU ``torch.Generator`` and rounded to the working dtype.
 Draw order inside one workload: Q, K, V, dO, then the valid key lengths.
 """
@@ -87,7 +88,7 @@ WORKLOADS = {
 def local_global_tile_mask(n_tiles: int, band: int = 4, n_global: int = 2) -> torch.Tensor:
     """uint8 [n_tiles, n_tiles]: tile (I, J) kept iff |I-J| <= band or I < n_global or J < n_global.
 
-    This is the sparsity *pattern* of the block-sparse workload (page 1, block-sparse
+    This is the sparsity *pattern* of the block-sparse workload ("FlashAttention paper story", block-sparse
     paragraph: local windows plus global tokens); it is input structure, not arithmetic.
     """
     idx = torch.arange(n_tiles)
