@@ -179,12 +179,64 @@ def max_over_ranks(values, device, world):
     return t.tolist()
 
 
+def needs_l2_flush(w):
+    """True when the forward's compulsory bytes are under twice the L2: timed back to back, such
+    inputs would stay warm in L2 from one step to the next."""
+    elt = 4 if w.dtype == "fp32" else 2
+    fwd, _ = compulsory_bytes(w.B, w.H, w.Hkv or w.H, w.N, w.d, elt)
+    return fwd < 2 * L2_BYTES
+
+
 def workload_config(w):
     return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv or w.H, "N": w.N, "d": w.d,
             "causal": w.causal,
             "key_padding": w.pad_lengths is not None, "block_sparse": w.block_sparse,
             "dtype": w.dtype, "parallelism": "replicas",
-            "l2": "inputs larger than L2 (no flush)"}
+            "l2": (f"L2 flushed between timed steps ({FLUSH_BYTES >> 20} MiB write, untimed)"
+                   if needs_l2_flush(w) else "inputs larger than L2 (no flush)")}
+
+
+L2_BYTES = 129_000_000             # GB300 L2, nominal
+FLUSH_BYTES = 256 * 2 ** 20         # written between timed steps when the inputs fit in L2
+
+
+def compulsory_bytes(B, H, Hkv, N, d, elt):
+    """Algorithmic HBM bytes of one forward and one backward (the compulsory traffic): the
+    forward reads Q, K, V and writes O and LSE; the backward reads Q, K, V, O, dO and LSE and
+    writes dQ, dK, dV."""
+    q_side = B * H * N * d * elt
+    kv_side = B * Hkv * N * d * elt
+    lse = B * H * N * 4
+    fwd = q_side + 2 * kv_side + q_side + lse
+    bwd = 3 * q_side + 2 * kv_side + lse + q_side + 2 * kv_side
+    return fwd, bwd
+
+
+def effective_forward_flops(w, x, B, H, N):
+    """Forward FLOPs over the allowed (query, key) pairs only: with key padding a row attends to
+    kv_len keys (the nominal count includes the padded ones the kernel skips)."""
+    if x["kv_lens"] is None:
+        return forward_flops(w, B, H, N, x["block_mask"])
+    lens = [int(v) for v in x["kv_lens"]]
+    if w.causal:
+        return sum(4.0 * H * w.d * sum(min(i + 1, L) for i in range(N)) for L in lens)
+    return sum(4.0 * H * w.d * N * L for L in lens)
+
+
+def peak_memory(fa, torch, q, k, v, do, kw, bkw):
+    """Device memory of one forward + backward through the public API: the inputs plus the
+    largest amount allocated during the calls (outputs, LSE, workspace), from the allocator's
+    own peak counter."""
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    o, lse = fa.forward(q, k, v, **kw)
+    grads = fa.backward(q, k, v, o, lse, do, **bkw)
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated() - base
+    del o, lse, grads
+    inputs = sum(t.numel() * t.element_size() for t in (q, k, v, do))
+    return inputs + peak, inputs, peak
 
 
 def run_ours(args, w):
@@ -206,20 +258,25 @@ def run_ours(args, w):
         if world > 1:
             dist.barrier()
 
-    if args.fused_backward:
-        fa.set_backward_variant(fa.BWD_FUSED_ATOMIC)
     x = make_inputs(w, seed=rank)
     B, H, N, d = x["q"].shape
+    Hkv = x["k"].shape[1]
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     bm = None if x["block_mask"] is None else x["block_mask"].to(dev)
     kl = None if x["kv_lens"] is None else x["kv_lens"].to(dev)
     o, lse = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(fa.backward_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    ws_bytes = (fa.backward_fused_workspace_size(B, H, N, d) if args.fused_backward
+                else fa.backward_workspace_size(B, H, N, d))
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     kw = dict(causal=w.causal, scale=w.scale, block_mask=bm, kv_lens=kl)
     if args.dropout > 0.0:
         kw.update(dropout_p=args.dropout, seed=1234, offset=0)
-    bkw = dict(kw, deterministic=args.deterministic)
+    bkw = dict(kw, deterministic=args.deterministic, fused=args.fused_backward)
+    fwd_bytes, bwd_bytes = compulsory_bytes(B, H, Hkv, N, d, q.element_size())
+    # Inputs that fit in L2 would be timed warm: then L2 is flushed between timed steps (a
+    # 256 MB write outside the timed events) and every step is timed on its own.
+    flush = needs_l2_flush(w)
 
     def step():
         fa.forward(q, k, v, o=o, lse=lse, **kw)
@@ -234,11 +291,17 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    scrub = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        if flush:
+            # hold the stream while every step is queued, so no step waits for the host
+            torch.cuda._sleep(int(2e8))
         start.record(stream)
         for i in range(args.steps):
+            if flush:
+                scrub.zero_()
             ev[i][0].record(stream)
             fa.forward(q, k, v, o=o, lse=lse, **kw)
             ev[i][1].record(stream)
@@ -247,9 +310,14 @@ def run_ours(args, w):
         end.record(stream)
         torch.cuda.synchronize()
     barrier()
-    total_ms = start.elapsed_time(end)
-    t_fwd = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
-    t_bwd = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    # with flushes, the timed work is the sum of the steps' own intervals (the flushes between
+    # them are not the method's work); without, the whole region between the two events
+    total_ms = sum(f + b for f, b in zip(fwd_ms, bwd_ms)) if flush else start.elapsed_time(end)
+    t_fwd = sum(fwd_ms) / args.steps
+    t_bwd = sum(bwd_ms) / args.steps
+    med_fwd, med_bwd = statistics.median(fwd_ms), statistics.median(bwd_ms)
     if fa.check_device_status() != 0:
         raise RuntimeError("device error during the timed region")
 
@@ -308,19 +376,37 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     barrier()
     e2e_ms = s2.elapsed_time(e2)
+    del bufs
 
-    total_ms, e2e_ms, t_fwd, t_bwd = max_over_ranks([total_ms, e2e_ms, t_fwd, t_bwd], dev, world)
+    mem_total, mem_inputs, mem_calls = peak_memory(fa, torch, q, k, v, do, kw, bkw)
+
+    total_ms, e2e_ms, t_fwd, t_bwd, med_fwd, med_bwd = max_over_ranks(
+        [total_ms, e2e_ms, t_fwd, t_bwd, med_fwd, med_bwd], dev, world)
 
     F = forward_flops(w, B, H, N, x["block_mask"])
+    F_eff = effective_forward_flops(w, x, B, H, N)
     ms_step = total_ms / args.steps
     value = world * 2.5 * F / (ms_step * 1e-3) / 1e12
     e2e_value = world * 2.5 * F / (e2e_ms / args.steps * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
     fwd_tf = F / (t_fwd * 1e-3) / 1e12
     bwd_tf = 2.5 * F / (t_bwd * 1e-3) / 1e12
     dominant = "backward" if t_bwd >= t_fwd else "forward"
-    achieved = bwd_tf if dominant == "backward" else fwd_tf
+    # roofline of the dominant call: max(F / F_peak, bytes / B_HBM) decides the bound; the
+    # achieved rate is reported in that bound's unit (effective FLOPs when keys are padded)
+    flops_dom = (2.5 if dominant == "backward" else 1.0) * F_eff
+    bytes_dom = bwd_bytes if dominant == "backward" else fwd_bytes
+    t_dom = (t_bwd if dominant == "backward" else t_fwd) * 1e-3
+    t_tensor, t_hbm = flops_dom / (peak * 1e12), bytes_dom / (hbm * 1e9)
+    if t_hbm > t_tensor:
+        roof = {"bound": "hbm", "achieved": bytes_dom / t_dom / 1e9, "peak": hbm, "unit": "GB/s",
+                "frac": bytes_dom / t_dom / 1e9 / hbm, "peak_source": f"hbm_gbs of {peak_src}"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops_dom / t_dom / 1e12, "peak": peak,
+                "unit": "TFLOP/s", "frac": flops_dom / t_dom / 1e12 / peak,
+                "peak_source": f"bf16_tflops of {peak_src}"}
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tp):
@@ -329,28 +415,46 @@ def run_ours(args, w):
         ent = rec.get(w.name, {}).get(dominant)
         if ent and ent.get("source_hash") == kernel_source_hash():
             traffic = ent.get("bytes_per_launch")
+    roof.update(kernel=f"fa_{dominant} (all launches of the call)", traffic=traffic)
+
+    def roofline_time_fraction(flops, nbytes, t_ms):
+        return max(flops / (peak * 1e12), nbytes / (hbm * 1e9)) / (t_ms * 1e-3)
+
+    config = dict(workload_config(w),
+                  backward="fused_atomic_dq" if args.fused_backward else "two_pass",
+                  **({"dropout": args.dropout} if args.dropout > 0.0 else {}))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": dict(workload_config(w),
-                       backward="fused_atomic_dq" if args.fused_backward else "two_pass",
-                       **({"dropout": args.dropout} if args.dropout > 0.0 else {})),
+        "config": config,
         "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
         "fwd_bwd_tflops_algorithmic": world * 3.5 * F / (ms_step * 1e-3) / 1e12,
         "pct_of_bf16_peak": {"forward": fwd_tf / peak, "fwd_bwd": value / world / peak,
                              "peak_tflops": peak, "peak_source": peak_src},
-        "ms_fwd": t_fwd, "ms_bwd": t_bwd,
-        "roofline": {"bound": "tensor", "kernel": f"fa_{dominant} (all launches of the call)",
-                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"bf16_tflops of {peak_src}"},
+        "ms_fwd": t_fwd, "ms_bwd": t_bwd, "ms_fwd_median": med_fwd, "ms_bwd_median": med_bwd,
+        "roofline_time_fraction": {
+            "forward": roofline_time_fraction(F_eff, fwd_bytes, med_fwd),
+            "backward": roofline_time_fraction(2.5 * F_eff, bwd_bytes, med_bwd),
+            "compulsory_bytes": {"forward": fwd_bytes, "backward": bwd_bytes},
+            "timing": "median of the per-step event times"},
+        "roofline": roof,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "pipelined": "copies in, compute and copies out on three streams, double-buffered",
                 "d2h_bytes_per_step": d2h},
+        "peak_mem_bytes": mem_total,
+        "peak_mem": {"inputs_bytes": mem_inputs, "allocated_by_the_calls_bytes": mem_calls,
+                     "workspace_bytes": ws_bytes,
+                     "bytes_per_q_row_element": mem_total / float(B * H * N * d),
+                     "one_fp32_score_matrix_bytes": 4 * B * H * N * N},
         "gpu_launches": LAUNCHES_PER_STEP["fused" if args.fused_backward else "two_pass"] * args.steps,
         "clocks": clocks.summary(),
     }
+    if F_eff != F:
+        line["effective_flops"] = {"forward_flops": F_eff, "nominal_forward_flops": F,
+                                   "fwd_tflops": F_eff / (t_fwd * 1e-3) / 1e12,
+                                   "bwd_tflops": 2.5 * F_eff / (t_bwd * 1e-3) / 1e12,
+                                   "note": "allowed (query, key) pairs only"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rows = min(N, args.cpu_rows)
         t_cpu = cpu_oracle_sample(x, w, rows)
@@ -511,7 +615,7 @@ def main():
     ap.add_argument("--deterministic", action="store_true",
                     help="call fa_backward_deterministic (the default two-pass backward, by name)")
     ap.add_argument("--fused-backward", action="store_true",
-                    help="time the fused atomic-dQ backward variant (fa_set_backward_variant)")
+                    help="time the fused atomic-dQ backward variant (fa_backward_fused)")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="dropout probability on P for the timed forward and backward")
     ap.add_argument("--splits", type=int, default=0,

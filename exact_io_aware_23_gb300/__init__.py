@@ -14,8 +14,9 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["forward", "forward_splitkv", "backward", "backward_noalloc", "backward_workspace_size", "check_device_status",
-           "set_fault_injection", "set_wait_limit_ms", "FaError", "LIB_PATH", "lib"]
+__all__ = ["forward", "forward_splitkv", "backward", "backward_noalloc", "backward_workspace_size",
+           "backward_fused_workspace_size", "check_device_status", "set_fault_injection",
+           "set_wait_limit_ms", "FaError", "LIB_PATH", "lib"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
 
@@ -78,8 +79,11 @@ def _load() -> ctypes.CDLL:
     L.fa_backward_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i,
                                       vp, dp, vp, sz, vp]
     L.fa_backward_dropout.restype = i
-    L.fa_set_backward_variant.argtypes = [i]
-    L.fa_set_backward_variant.restype = i
+    L.fa_backward_fused.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i,
+                                    vp, vp, sz, vp]
+    L.fa_backward_fused.restype = i
+    L.fa_backward_fused_workspace_size.argtypes = [i, i, i, i]
+    L.fa_backward_fused_workspace_size.restype = sz
     L.fa_forward_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, i, vp, sz, vp]
     L.fa_forward_splitkv_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, i, i, vp, sz, vp]
     L.fa_forward_splitkv_gqa.restype = i
@@ -279,12 +283,17 @@ def backward_deterministic_workspace_size(B: int, H: int, N: int) -> int:
     return int(lib.fa_backward_deterministic_workspace_size(B, H, N))
 
 
+def backward_fused_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(lib.fa_backward_fused_workspace_size(B, H, N, d))
+
+
 def backward(q, k, v, o, lse, do, *, causal: bool = False, scale: Optional[float] = None,
              block_mask=None, kv_lens=None, dq=None, dk=None, dv=None, workspace=None,
-             stream=None, deterministic: bool = False, dropout_p: float = 0.0, seed: int = 0,
-             offset: int = 0):
+             stream=None, deterministic: bool = False, fused: bool = False,
+             dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
     """dQ, dK, dV = recompute-based attention backward (fa_backward; fa_backward_gqa when k, v
-    have fewer heads than q; fa_backward_deterministic, bit-reproducible, when asked)."""
+    have fewer heads than q; fa_backward_deterministic, bit-reproducible, when asked;
+    fa_backward_fused, the single-pass atomic-dQ variant, when asked)."""
     B, H, N, d, Hkv = _check_qkv(q, k, v)
     for name, t in (("o", o), ("do", do)):
         if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
@@ -296,7 +305,10 @@ def backward(q, k, v, o, lse, do, *, causal: bool = False, scale: Optional[float
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    need = (backward_deterministic_workspace_size(B, H, N) if deterministic or dropout_p > 0.0
+    if fused and (deterministic or dropout_p > 0.0):
+        raise ValueError("the fused backward has no deterministic or dropout form")
+    need = (backward_fused_workspace_size(B, H, N, d) if fused
+            else backward_deterministic_workspace_size(B, H, N) if deterministic or dropout_p > 0.0
             else backward_workspace_size(B, H, N, d))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
@@ -316,6 +328,11 @@ def backward(q, k, v, o, lse, do, *, causal: bool = False, scale: Optional[float
         st = lib.fa_backward_deterministic(*args, B, H, Hkv, N, *tail)
         if st != FA_OK:
             raise FaError(st, "fa_backward_deterministic")
+        return dq, dk, dv
+    if fused:
+        st = lib.fa_backward_fused(*args, B, H, Hkv, N, *tail)
+        if st != FA_OK:
+            raise FaError(st, "fa_backward_fused")
         return dq, dk, dv
     if Hkv == H:
         st = lib.fa_backward(*args, B, H, N, *tail)
@@ -337,16 +354,6 @@ def set_fault_injection(mode: int) -> None:
 
 def set_wait_limit_ms(ms: int) -> None:
     lib.fa_debug_set_wait_limit_ms(int(ms))
-
-
-BWD_TWO_PASS, BWD_FUSED_ATOMIC = 0, 1
-
-
-def set_backward_variant(variant: int) -> None:
-    """fa_set_backward_variant: BWD_TWO_PASS (default, deterministic) or BWD_FUSED_ATOMIC."""
-    st = lib.fa_set_backward_variant(int(variant))
-    if st != FA_OK:
-        raise FaError(st, "fa_set_backward_variant")
 
 
 def backward_noalloc(q, k, v, o, lse, do, *, causal: bool = False, scale: Optional[float] = None,

@@ -14,21 +14,16 @@ namespace {
 // Per-device error word written by kernels whose bounded waits ran out.
 __device__ int g_fa_error_word;
 
-constexpr int kMaxDevices = 64;
-int* g_err_ptr[kMaxDevices] = {nullptr};
+fa::SymbolCache g_err_cache;
+// Test hooks of the failure-detection path (process-wide; see fa_debug_set_fault_injection).
 std::atomic<int> g_inject{0};
 std::atomic<uint32_t> g_wait_limit_ms{2000};
-std::atomic<int> g_bwd_variant{FA_BWD_TWO_PASS};
 
+// The error word of the current context (looked up once per context).
 fa_status device_error_word(int** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
-  if (g_err_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_fa_error_word) != cudaSuccess) return FA_ERR_CUDA;
-    g_err_ptr[dev] = static_cast<int*>(p);
-  }
-  *out = g_err_ptr[dev];
+  void* p = nullptr;
+  if (fa::symbol_address(g_err_cache, (const void*)&g_fa_error_word, &p) != cudaSuccess) return FA_ERR_CUDA;
+  *out = static_cast<int*>(p);
   return FA_OK;
 }
 
@@ -71,7 +66,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 extern "C" {
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 200; }
 
 const char* fa_status_string(fa_status s) {
   switch (s) {
@@ -87,12 +82,6 @@ const char* fa_status_string(fa_status s) {
 void fa_debug_set_fault_injection(int mode) { g_inject.store(mode); }
 
 void fa_debug_set_wait_limit_ms(uint32_t ms) { g_wait_limit_ms.store(ms == 0 ? 2000u : ms); }
-
-fa_status fa_set_backward_variant(fa_bwd_variant v) {
-  if (v != FA_BWD_TWO_PASS && v != FA_BWD_FUSED_ATOMIC) return FA_ERR_INVALID_ARG;
-  g_bwd_variant.store(v);
-  return FA_OK;
-}
 
 }  // extern "C"
 
@@ -248,8 +237,7 @@ fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* 
 
 size_t fa_backward_workspace_size(int B, int H, int N, int d) {
   if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
-  const size_t rows = (size_t)B * H * N;
-  return round_up(rows * (size_t)d * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+  return round_up((size_t)B * H * N * sizeof(float), 256);   // D only: no dQ accumulator
 }
 
 size_t fa_backward_deterministic_workspace_size(int B, int H, int N) {
@@ -257,28 +245,38 @@ size_t fa_backward_deterministic_workspace_size(int B, int H, int N) {
   return round_up((size_t)B * H * N * sizeof(float), 256);   // D only: no dQ accumulator
 }
 
+size_t fa_backward_fused_workspace_size(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
+  const size_t rows = (size_t)B * H * N;
+  return round_up(rows * (size_t)d * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+}
+
 }  // extern "C"
 
 namespace {
+
+// Which backward runs: kAuto = the two-pass kernel for 16-bit inputs and the CUDA-core kernel
+// for fp32; kTwoPass = the two-pass kernel only (fp32 unsupported); kFused = the key-stationary
+// kernel that adds dQ into an fp32 workspace (16-bit only).
+enum class BwdPath { kAuto, kTwoPass, kFused };
 
 fa_status backward_impl(const void* q, const void* k, const void* v, const void* o,
                         const void* dO, const float* lse, void* dq, void* dk, void* dv,
                         int B, int H, int Hkv, int N, int d, float scale, int causal,
                         const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
                         void* workspace, size_t workspace_bytes, void* stream,
-                        bool deterministic, Packing pk = {nullptr, 0}, fa::DropoutArgs drop = {}) {
+                        BwdPath path, Packing pk = {nullptr, 0}, fa::DropoutArgs drop = {}) {
   fa_status st = check_common(B, H, N, d, scale, dtype);
   if (st != FA_OK) return st;
   st = check_heads(H, Hkv, dtype);
   if (st != FA_OK) return st;
-  if ((deterministic || pk.cu_seqlens != nullptr || drop.enabled) && dtype == FA_FP32)
+  if ((path != BwdPath::kAuto || pk.cu_seqlens != nullptr || drop.enabled) && dtype == FA_FP32)
     return FA_ERR_UNSUPPORTED;
   if (pk.cu_seqlens != nullptr && drop.enabled) return FA_ERR_UNSUPPORTED;
-  // 16-bit inputs run the two-pass backward unless the fused one was selected (packed sequences
-  // always take the two-pass one); fp32 always runs the CUDA-core backward (which adds dQ from
-  // several blocks).
-  const bool two_pass = deterministic || pk.cu_seqlens != nullptr || drop.enabled ||
-                        (dtype != FA_FP32 && g_bwd_variant.load() == FA_BWD_TWO_PASS);
+  // 16-bit inputs run the two-pass backward unless the fused one was asked for; fp32 always runs
+  // the CUDA-core backward, which adds dQ from several blocks into the fp32 dQ output itself.
+  const bool fused = path == BwdPath::kFused;
+  const bool two_pass = !fused && dtype != FA_FP32;
   // workspace sizes count the query rows of all slices: B*H*N, or H*total when packed
   const int wB = pk.cu_seqlens != nullptr ? 1 : B, wN = pk.cu_seqlens != nullptr ? pk.total : N;
   if (B == 0 || H == 0 || N == 0 || (pk.cu_seqlens != nullptr && pk.total == 0)) return FA_OK;
@@ -289,14 +287,17 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
       !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
-  const size_t need = deterministic ? fa_backward_deterministic_workspace_size(wB, H, wN)
-                                    : fa_backward_workspace_size(wB, H, wN, d);
+  const size_t need = fused ? fa_backward_fused_workspace_size(wB, H, wN, d)
+                            : fa_backward_workspace_size(wB, H, wN, d);
   if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.o = o; a.dO = dO; a.lse = lse; a.dq = dq; a.dk = dk; a.dv = dv;
   const size_t rows = (size_t)wB * H * wN;
   if (two_pass) {                      // D only: dQ is written once, no accumulator
     a.dq_acc = nullptr;
+    a.delta = static_cast<float*>(workspace);
+  } else if (!fused) {                 // fp32: the fp32 dQ output is its own accumulator
+    a.dq_acc = static_cast<float*>(dq);
     a.delta = static_cast<float*>(workspace);
   } else {
     a.dq_acc = static_cast<float*>(workspace);
@@ -337,7 +338,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                       const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
                       void* workspace, size_t workspace_bytes, void* stream) {
   return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, N, d, scale, causal, block_mask,
-                       dtype, kv_lens, workspace, workspace_bytes, stream, false);
+                       dtype, kv_lens, workspace, workspace_bytes, stream, BwdPath::kAuto);
 }
 
 fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const void* o,
@@ -346,7 +347,16 @@ fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const voi
                           const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
                           void* workspace, size_t workspace_bytes, void* stream) {
   return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal, block_mask,
-                       dtype, kv_lens, workspace, workspace_bytes, stream, false);
+                       dtype, kv_lens, workspace, workspace_bytes, stream, BwdPath::kAuto);
+}
+
+fa_status fa_backward_fused(const void* q, const void* k, const void* v, const void* o,
+                            const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                            int B, int H, int Hkv, int N, int d, float scale, int causal,
+                            const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal, block_mask,
+                       dtype, kv_lens, workspace, workspace_bytes, stream, BwdPath::kFused);
 }
 
 fa_status fa_backward_deterministic(const void* q, const void* k, const void* v, const void* o,
@@ -356,7 +366,7 @@ fa_status fa_backward_deterministic(const void* q, const void* k, const void* v,
                                     const int32_t* kv_lens, void* workspace,
                                     size_t workspace_bytes, void* stream) {
   return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal, block_mask,
-                       dtype, kv_lens, workspace, workspace_bytes, stream, true);
+                       dtype, kv_lens, workspace, workspace_bytes, stream, BwdPath::kTwoPass);
 }
 
 fa_status fa_forward_splitkv_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -396,8 +406,8 @@ fa_status fa_backward_dropout(const void* q, const void* k, const void* v, const
   const fa_status st = make_dropout(dropout, &drop);
   if (st != FA_OK) return st;
   return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal, block_mask,
-                       dtype, kv_lens, workspace, workspace_bytes, stream, true, Packing{nullptr, 0},
-                       drop);
+                       dtype, kv_lens, workspace, workspace_bytes, stream, BwdPath::kTwoPass,
+                       Packing{nullptr, 0}, drop);
 }
 
 fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -418,8 +428,8 @@ fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const 
   if (n_seqs < 0 || max_seqlen < 0 || total < 0) return FA_ERR_INVALID_ARG;
   if (n_seqs > 0 && total > 0 && cu_seqlens == nullptr) return FA_ERR_INVALID_ARG;
   return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, n_seqs, H, Hkv, max_seqlen, d, scale,
-                       causal, nullptr, dtype, nullptr, workspace, workspace_bytes, stream, true,
-                       Packing{cu_seqlens, total});
+                       causal, nullptr, dtype, nullptr, workspace, workspace_bytes, stream,
+                       BwdPath::kTwoPass, Packing{cu_seqlens, total});
 }
 
 fa_status fa_check_device_status(void* stream) {

@@ -1,25 +1,25 @@
 // fa_backward_noalloc: the backward for callers that cannot allocate device memory.
 //
-// fa_backward needs a caller-provided scratch workspace (the fp32 dQ accumulator and the
-// per-row D vector).  Some callers have no way to provide one: plugin interfaces that hand
-// over only input and output pointers, hosts whose memory is entirely reserved by their own
-// allocator, and latency-critical paths that may not call cudaMalloc because it synchronises
-// the device.  This entry point takes its scratch from a fixed array compiled into the
-// library instead, so it allocates nothing.
+// fa_backward needs a caller-provided scratch workspace (the per-row D = rowsum(dO * O)).
+// Some callers have no way to provide one: plugin interfaces that hand over only input and
+// output pointers, hosts whose memory is entirely reserved by their own allocator, and
+// latency-critical paths that may not call cudaMalloc because it synchronises the device.  This
+// entry point takes its scratch from a fixed array compiled into the library instead, so it
+// allocates nothing.
 //
 // The array lives in device memory of every GPU that loads the library, for the life of the
-// process.  Its device address is looked up once per device (cudaGetSymbolAddress, with that
-// device current) on the first call made on the device; make that first call before any
-// stream capture.  Every call shares the one array, so two calls that overlap on the GPU
-// (different streams, or different host threads) race on it; serialise them.  Nothing needs
-// to be cleared between calls: the backward zeroes its dQ accumulator and rewrites D on every
-// call.
+// process.  Its device address is looked up (cudaGetSymbolAddress) by the first call made in
+// each CUDA context, with that context current, and cached for that context; make that first
+// call before any stream capture.  A device reset (cudaDeviceReset) is not supported: the
+// primary context can come back under the same handle, and the cached address would be stale.
+// Every call shares the one array, so two calls that overlap on the GPU (different streams, or
+// different host threads) race on it; serialise them.  Nothing needs to be cleared between
+// calls: every call rewrites D for each row before reading it.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "../../include/fa.h"
+#include "fa_sm103.cuh"
 
 namespace {
 
@@ -27,21 +27,12 @@ constexpr size_t kScratchBytes = size_t(32) << 20;   // 32 MiB
 
 static __device__ __align__(256) uint8_t g_bwd_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
-std::mutex g_scratch_mu;
+fa::SymbolCache g_scratch_cache;
 
-// Device address of the scratch array on the current device (resolved once per device).
+// Device address of the scratch array in the current context (looked up once per context).
 fa_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  if (fa::symbol_address(g_scratch_cache, (const void*)g_bwd_scratch, out) != cudaSuccess)
+    return FA_ERR_CUDA;
   return FA_OK;
 }
 

@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "fa_internal.cuh"
 
 namespace fa {
@@ -25,5 +27,23 @@ cudaError_t encode_tensor_map(CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t
                               const void* base, const cuuint64_t* dims, const cuuint64_t* strides,
                               const cuuint32_t* box, const cuuint32_t* elem_strides,
                               CUtensorMapSwizzle swizzle);
+
+// Device addresses of one of the library's __device__ variables, one per CUDA context that
+// looked it up (a context is where a module's globals live: another device, or another context
+// on the same device, has its own copy).  A context destroyed while the process runs (for
+// example by cudaDeviceReset) can come back under the same handle; its cached address is then
+// stale, so the library does not support further calls on a device after a reset.
+struct SymbolCache {
+  static constexpr int kEntries = 64;
+  std::mutex mu;
+  void* ctx[kEntries] = {nullptr};
+  void* ptr[kEntries] = {nullptr};
+  int n = 0;
+  int next = 0;
+};
+
+// The device address of `symbol` in the calling thread's current context (looked up with
+// cudaGetSymbolAddress on the first call in that context, cached afterwards).
+cudaError_t symbol_address(SymbolCache& cache, const void* symbol, void** out);
 
 }  // namespace fa

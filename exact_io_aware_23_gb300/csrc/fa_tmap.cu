@@ -28,7 +28,60 @@ void resolve() {
     g_encode = reinterpret_cast<EncodeFn>(fn);
 }
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn g_ctx_get = nullptr;
+std::once_flag g_ctx_once;
+
+void resolve_ctx() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_ctx_get = reinterpret_cast<CtxGetCurrentFn>(fn);
+}
+
+// The calling thread's current CUDA context (null when none is current yet).
+cudaError_t current_context(void** ctx) {
+  std::call_once(g_ctx_once, resolve_ctx);
+  *ctx = nullptr;
+  if (g_ctx_get == nullptr) return cudaErrorNotSupported;
+  CUcontext c = nullptr;
+  if (g_ctx_get(&c) != CUDA_SUCCESS) return cudaErrorUnknown;
+  *ctx = static_cast<void*>(c);
+  return cudaSuccess;
+}
+
 }  // namespace
+
+cudaError_t symbol_address(SymbolCache& cache, const void* symbol, void** out) {
+  *out = nullptr;
+  void* ctx = nullptr;
+  cudaError_t e = current_context(&ctx);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(cache.mu);
+  if (ctx != nullptr) {
+    for (int i = 0; i < cache.n; ++i) {
+      if (cache.ctx[i] == ctx) {
+        *out = cache.ptr[i];
+        return cudaSuccess;
+      }
+    }
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, symbol);
+  if (e != cudaSuccess) return e;
+  if (p == nullptr) return cudaErrorInvalidSymbol;
+  if (ctx == nullptr && current_context(&ctx) != cudaSuccess) ctx = nullptr;   // the lookup made
+                                                                              // a context current
+  if (ctx != nullptr) {
+    const int slot = cache.n < SymbolCache::kEntries ? cache.n++ : (cache.next++ % SymbolCache::kEntries);
+    cache.ctx[slot] = ctx;
+    cache.ptr[slot] = p;
+  }
+  *out = p;
+  return cudaSuccess;
+}
 
 cudaError_t encode_tensor_map(CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank,
                               const void* base, const cuuint64_t* dims, const cuuint64_t* strides,

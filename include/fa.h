@@ -28,8 +28,11 @@
  *   - LSE: float32 [B, H, N], natural log.  kv_lens: int32 [B].  block_mask: uint8 [T, T],
  *     row-major, one mask for every (b, h).  All device pointers.
  *   - d must be 64 or 128.  N >= 1 (B, H or N equal to 0 is a no-op returning FA_OK).
- *   - The library allocates no device memory.  The backward's scratch (fp32 dQ accumulator
- *     and the per-row D = rowsum(dO * O)) is the caller's workspace.
+ *   - The library allocates no device memory.  The backward's scratch (the per-row
+ *     D = rowsum(dO * O), and for fa_backward_fused also an fp32 dQ accumulator) is the
+ *     caller's workspace.
+ *   - No call depends on process-wide state set by another call, except the two test hooks at
+ *     the end of this header.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).  A
  *     return of FA_OK means the kernels were launched.  Argument errors are detected on the
  *     host before anything is launched.  No call aborts or throws.
@@ -216,7 +219,9 @@ size_t fa_forward_splitkv_workspace_size(int B, int H, int Nq, int d, int n_spli
  * to 95 %; at least two key tiles per range, at most 64 ranges. */
 int fa_forward_splitkv_auto_splits(int B, int H, int Nq, int Nk);
 
-/* Bytes of workspace fa_backward needs for these sizes (a multiple of 256). */
+/* Bytes of workspace fa_backward, fa_backward_gqa and fa_backward_noalloc's path need for these
+ * sizes: one fp32 per query row for D (B*H*N*4, rounded up to a multiple of 256).  d is not used;
+ * it is kept so that the size is asked for with the problem's own sizes. */
 size_t fa_backward_workspace_size(int B, int H, int N, int d);
 
 /*
@@ -233,8 +238,9 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d);
  *                 and are overwritten.  Two calls in flight at once need two workspaces.
  * Other arguments as in fa_forward.  bf16 and fp16 run the two-pass backward of
  * fa_backward_deterministic (dK/dV over key tiles, dQ over query tiles, no cross-block sums):
- * the same bits on every run.  fp32, and the fused variant that fa_set_backward_variant can
- * select, add dQ from several blocks in an order that varies in the last bits.
+ * the same bits on every run.  fp32 runs on the CUDA cores and adds dQ from several blocks
+ * into the fp32 dq output (which doubles as its accumulator), in an order that varies in the
+ * last bits.
  */
 fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
                       const void* dO, const float* lse, void* dq, void* dk, void* dv,
@@ -249,11 +255,14 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
  * synchronises the device) is not allowed.  The pages have no counterpart of this call.
  * The scratch comes from a fixed array of fa_backward_noalloc_max_workspace() bytes (32 MiB)
  * built into the library; every GPU that loads the library holds it until the process exits.
- * Arguments and results are those of fa_backward.  Returns FA_ERR_UNSUPPORTED, launching
- * nothing, when fa_backward_workspace_size(B, H, N, d) exceeds that size.  The first call on a
- * device looks up the array's device address; make it before any stream capture.  All calls
- * share the array: calls that overlap on the GPU race on it and must be serialised.  Nothing
- * carries over between calls (the dQ accumulator is zeroed by every call).
+ * Arguments and results are those of fa_backward (the same path: two-pass for bf16/fp16,
+ * CUDA cores for fp32).  Returns FA_ERR_UNSUPPORTED, launching nothing, when
+ * fa_backward_workspace_size(B, H, N, d) exceeds that size (more than 8 388 608 query rows
+ * B*H*N).  The first call in a CUDA context looks up the array's device address and caches it
+ * for that context; make it before any stream capture.  Not supported after cudaDeviceReset on
+ * the device (the cached address can be stale).  All calls share the array: calls that overlap
+ * on the GPU race on it and must be serialised.  Nothing carries over between calls: every call
+ * rewrites D for each row before reading it.
  */
 fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o,
                               const void* dO, const float* lse, void* dq, void* dk, void* dv,
@@ -276,27 +285,34 @@ fa_status fa_check_device_status(void* stream);
 const char* fa_status_string(fa_status s);
 
 /*
- * Test hooks for the failure-detection path (no fault is involved).  mode 1 makes the next
- * launches of the tensor-core forward skip issuing their first K/V tile load, so the
- * consumers' bounded waits run out; the kernel then records FA_ERR_TIMEOUT and returns
- * normally.  wait_limit_ms sets the bound of every such wait (default 2000 ms; 0 restores it).
- * Both settings are process-wide.
+ * Test hooks for the failure-detection path (no fault is involved); not for production use.
+ * mode 1 makes the next launches of the tensor-core forward skip issuing their first K/V tile
+ * load, so the consumers' bounded waits run out; the kernel then records FA_ERR_TIMEOUT and
+ * returns normally.  wait_limit_ms sets the bound of every such wait (default 2000 ms; 0
+ * restores it).  Both settings are process-wide and change every later launch from every host
+ * thread: a test that sets them must restore them (mode 0, limit 0) before other work runs.
  */
 void fa_debug_set_fault_injection(int mode);
 void fa_debug_set_wait_limit_ms(uint32_t wait_limit_ms);
 
 /*
- * Backward variant for bf16/fp16 inputs of fa_backward, fa_backward_gqa and
- * fa_backward_noalloc (process-wide; fp32 is unaffected):
- *   FA_BWD_TWO_PASS      (default) the two passes of fa_backward_deterministic in one launch;
- *   FA_BWD_FUSED_ATOMIC  one key-stationary kernel computing dK, dV and dQ, dQ added into an fp32
- *                        workspace by the TMA unit from every key tile (fewer matrix products,
- *                        nondeterministic last bits; slower on most shapes on GB300).
- * Returns FA_ERR_INVALID_ARG for any other value.  No counterpart in the pages: they describe
- * one backward and leave its work partition open.
+ * The backward as one key-stationary kernel that computes dK, dV and dQ together, the work
+ * partition of the pages' single-pass backward ("FlashAttention paper story", backward
+ * paragraph): each key tile's share of dQ is added into an fp32 accumulator in the workspace by
+ * the TMA unit (bulk tensor reduce-add), then scaled and converted.  Five matrix products per
+ * tile pair instead of the two-pass kernel's seven, but the additions from several CTAs land in
+ * an order that varies in the last bits of dQ, and on GB300 it measures slower than the two-pass
+ * backward on most shapes.  bf16 or fp16 (FA_ERR_UNSUPPORTED for fp32); grouped heads as in
+ * fa_backward_gqa.  workspace: at least fa_backward_fused_workspace_size(B, H, N, d) bytes
+ * (fp32 dQ accumulator [B,H,N,d], then D), 256-byte aligned, caller-owned, contents on entry
+ * irrelevant.  Other arguments, errors and ownership as in fa_backward.
  */
-typedef enum { FA_BWD_TWO_PASS = 0, FA_BWD_FUSED_ATOMIC = 1 } fa_bwd_variant;
-fa_status fa_set_backward_variant(fa_bwd_variant variant);
+size_t fa_backward_fused_workspace_size(int B, int H, int N, int d);
+fa_status fa_backward_fused(const void* q, const void* k, const void* v, const void* o,
+                            const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                            int B, int H, int Hkv, int N, int d, float scale, int causal,
+                            const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                            void* workspace, size_t workspace_bytes, void* stream);
 
 /* ABI version of this header: major * 100 + minor. */
 int fa_version(void);

@@ -13,6 +13,7 @@ import numpy as np
 import torch
 
 import oracle
+from ideal_kernel import ideal_backward, ideal_forward
 from tolerances import (FP32_MAX_ABS, assert_bf16_close, assert_fp32_close, assert_lse_close)
 
 LSE_TOL_BF16 = 1e-3   # LSE is computed in fp32 from exact bf16 products; it is not rounded to bf16
@@ -36,14 +37,14 @@ def _dev(x):
     return q, k, v, do, dict(causal=x["causal"], scale=x["scale"], block_mask=bm, kv_lens=kl)
 
 
-def run_gpu(x, backward=True, deterministic=False):
+def run_gpu(x, backward=True, deterministic=False, fused=False):
     """Chained GPU forward (and backward on the forward's own O, LSE)."""
     import exact_io_aware_23_gb300 as fa
     q, k, v, do, kw = _dev(x)
     o, lse = fa.forward(q, k, v, **kw)
     out = dict(o=o, lse=lse)
     if backward:
-        dq, dk, dv = fa.backward(q, k, v, o, lse, do, deterministic=deterministic, **kw)
+        dq, dk, dv = fa.backward(q, k, v, o, lse, do, deterministic=deterministic, fused=fused, **kw)
         out.update(dq=dq, dk=dk, dv=dv)
     assert fa.check_device_status() == 0
     return out
@@ -70,7 +71,7 @@ def compare_fwd(x, out, heads=None, rows=None, ref=None):
         assert np.array_equal(np.isneginf(gl), neg)
         res["LSE"] = assert_fp32_close("LSE", gl[~neg], L[~neg])
     else:
-        res["O"] = assert_bf16_close("O", go, O)
+        res["O"] = assert_bf16_close("O", go, O, ideal=ideal_forward(x, heads=hs, rows=rows))
         res["LSE"] = assert_lse_close(gl, L, LSE_TOL_BF16)
     return res
 
@@ -85,13 +86,15 @@ def compare_bwd(x, grads, heads=None, o_given=None):
                                  block_mask=bm, heads=hs, o=og)
     grouped = kk.shape[1] != H          # dK, dV then hold the key/value heads' group sums
     assert not (grouped and heads is not None)
+    ideal = (None, None, None) if x["dtype"] == "fp32" else ideal_backward(x, heads=hs, o=og)
     res = {}
-    for name, key, ref in (("dQ", "dq", dQ), ("dK", "dk", dK), ("dV", "dv", dV)):
+    for name, key, ref, idl in (("dQ", "dq", dQ, ideal[0]), ("dK", "dk", dK, ideal[1]),
+                                ("dV", "dv", dV, ideal[2])):
         got = f64(grads[key]) if grouped and key != "dq" else f64(grads[key])[:, hs]
         if x["dtype"] == "fp32":
             res[name] = assert_fp32_close(name, got, ref, FP32_MAX_ABS)
         else:
-            res[name] = assert_bf16_close(name, got, ref)
+            res[name] = assert_bf16_close(name, got, ref, ideal=idl)
     return res
 
 
@@ -103,7 +106,7 @@ def compare(x, out, heads=None, rows=None, backward=True):
     return res
 
 
-def check_backward_given_o(x, deterministic=False):
+def check_backward_given_o(x, deterministic=False, fused=False):
     """GPU backward on the oracle's O (rounded to the working dtype) and LSE, against the
     oracle's backward for that O; forward checked separately."""
     import exact_io_aware_23_gb300 as fa
@@ -114,6 +117,6 @@ def check_backward_given_o(x, deterministic=False):
     q, k, v, do, kw = _dev(x)
     dev = q.device
     dq, dk, dv = fa.backward(q, k, v, o_in.to(dev), lse_in.to(dev), do, deterministic=deterministic,
-                             **kw)
+                             fused=fused, **kw)
     assert fa.check_device_status() == 0
     return compare_bwd(x, dict(dq=dq, dk=dk, dv=dv), o_given=o_in.to(torch.float64).numpy())

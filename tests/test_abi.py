@@ -54,7 +54,7 @@ def test_status_strings(lib):
     assert lib.fa_status_string(0) == b"FA_OK"
     assert lib.fa_status_string(4) == b"FA_ERR_TIMEOUT"
     assert lib.fa_status_string(99) == b"FA_UNKNOWN_STATUS"
-    assert lib.fa_version() == 100
+    assert lib.fa_version() == 200
 
 
 P = ctypes.c_void_p(0x10000)       # aligned, never dereferenced: every call below returns early
@@ -89,8 +89,9 @@ def test_forward_argument_checks(lib):
 
 def test_backward_argument_checks(lib):
     ws = lib.fa_backward_workspace_size(2, 3, 100, 64)
-    assert ws % 256 == 0 and ws >= 2 * 3 * 100 * 64 * 4 + 2 * 3 * 100 * 4
+    assert ws % 256 == 0 and 2 * 3 * 100 * 4 <= ws < 2 * 3 * 100 * 4 + 256     # D only
     assert lib.fa_backward_workspace_size(0, 3, 100, 64) == 0
+    assert lib.fa_backward_workspace_size(1, 16, 16384, 128) == 1 << 20   # the long workload: 1 MiB
 
     def bwd(dq=P, workspace=P, wsb=ws, d=64, N=100, dtype=0):
         return lib.fa_backward(P, P, P, P, P, P, dq, P, P, 2, 3, N, d, 0.125, 0, None, dtype, None,
@@ -192,7 +193,7 @@ def test_deterministic_backward_argument_checks(lib):
     lib.fa_backward_deterministic_workspace_size.restype = sz
     ws = lib.fa_backward_deterministic_workspace_size(2, 8, 100)
     assert ws % 256 == 0 and ws >= 2 * 8 * 100 * 4
-    assert ws < lib.fa_backward_workspace_size(2, 8, 100, 64)      # no dQ accumulator
+    assert ws == lib.fa_backward_workspace_size(2, 8, 100, 64)     # no dQ accumulator
     assert lib.fa_backward_deterministic_workspace_size(0, 8, 100) == 0
 
     def call(Hkv=8, N=100, dtype=0, wsb=ws, w=P, d=64):
@@ -208,12 +209,29 @@ def test_deterministic_backward_argument_checks(lib):
     assert call(N=0) == OK
 
 
-def test_backward_variant_selector(lib):
-    lib.fa_set_backward_variant.argtypes = [ctypes.c_int]
-    assert lib.fa_set_backward_variant(2) == INVALID
-    assert lib.fa_set_backward_variant(-1) == INVALID
-    assert lib.fa_set_backward_variant(1) == OK
-    assert lib.fa_set_backward_variant(0) == OK           # back to the default
+def test_fused_backward_argument_checks(lib):
+    """The fused single-pass backward is its own entry point with its own, larger workspace (fp32
+    dQ accumulator + D); no process-wide switch selects it."""
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_backward_fused.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp,
+                                      i, vp, vp, sz, vp]
+    lib.fa_backward_fused_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_backward_fused_workspace_size.restype = sz
+    ws = lib.fa_backward_fused_workspace_size(2, 8, 100, 64)
+    assert ws % 256 == 0 and ws >= 2 * 8 * 100 * 64 * 4 + 2 * 8 * 100 * 4
+    assert lib.fa_backward_fused_workspace_size(2, 8, 100, 0) == 0
+    assert "fa_set_backward_variant" not in declared_functions()
+
+    def call(Hkv=8, N=100, dtype=0, wsb=ws, w=P, d=64):
+        return lib.fa_backward_fused(P, P, P, P, P, P, P, P, P, 2, 8, Hkv, N, d, 0.125, 1, None,
+                                     dtype, None, w, wsb, None)
+    assert call(dtype=1) == UNSUPPORTED
+    assert call(d=96) == UNSUPPORTED
+    assert call(Hkv=3) == UNSUPPORTED
+    assert call(w=None) == INVALID
+    assert call(wsb=lib.fa_backward_workspace_size(2, 8, 100, 64)) == INVALID   # D only: too small
+    assert call(wsb=ws - 4) == INVALID
+    assert call(N=0) == OK
 
 
 def test_varlen_argument_checks(lib):

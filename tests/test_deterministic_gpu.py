@@ -12,6 +12,7 @@ import torch
 
 import oracle
 from gpu_helpers import _dev, check_backward_given_o, compare, compare_bwd, f64, run_gpu
+from ideal_kernel import ideal_backward
 from tolerances import assert_bf16_close
 from workloads import WORKLOADS, Workload, make_inputs, random_tile_mask
 
@@ -47,18 +48,6 @@ def test_deterministic_grouped_heads(Hkv):
     compare(x, run_gpu(x, deterministic=True))
 
 
-class _FusedVariant:
-    """Selects the fused atomic-dQ backward for the block (process-wide), then restores."""
-
-    def __enter__(self):
-        import exact_io_aware_23_gb300 as fa
-        fa.set_backward_variant(fa.BWD_FUSED_ATOMIC)
-
-    def __exit__(self, *exc):
-        import exact_io_aware_23_gb300 as fa
-        fa.set_backward_variant(fa.BWD_TWO_PASS)
-
-
 def _both(x, reps=3):
     import exact_io_aware_23_gb300 as fa
     q, k, v, do, kw = _dev(x)
@@ -67,8 +56,7 @@ def _both(x, reps=3):
     default = fa.backward(q, k, v, o, lse, do, **kw)
     for a_, b_ in zip(det[0], default):
         assert torch.equal(a_, b_)
-    with _FusedVariant():
-        fused = fa.backward(q, k, v, o, lse, do, **kw)
+    fused = fa.backward(q, k, v, o, lse, do, fused=True, **kw)
     assert fa.check_device_status() == 0
     return det, fused
 
@@ -99,30 +87,37 @@ def test_long_causal_n16k_d128():
     heads = [0, 9]
     qq, kk, vv, dd = (f64(x[n]) for n in ("q", "k", "v", "do"))
     dQ, _, _ = oracle.backward(qq, kk, vv, dd, x["scale"], causal=True, heads=heads, rows=rows)
-    assert_bf16_close("dQ", f64(det[0][0])[:, heads][:, :, rows], dQ[:, :, rows])
+    idq = ideal_backward(x, heads=heads, rows=rows)[0]
+    assert_bf16_close("dQ", f64(det[0][0])[:, heads][:, :, rows], dQ[:, :, rows], ideal=idq[:, :, rows])
 
 
-# --- the fused atomic-dQ variant (fa_set_backward_variant) ----------------------------------
+# --- the fused atomic-dQ variant (fa_backward_fused) -----------------------------------------
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N,causal", [(300, True), (1000, False)])
 def test_fused_variant_shapes(N, d, causal):
     x = _case(N, d, causal=causal, seed=7 * N + d)
-    with _FusedVariant():
-        compare(x, run_gpu(x))
-        check_backward_given_o(x)
+    compare(x, run_gpu(x, fused=True))
+    check_backward_given_o(x, fused=True)
 
 
 def test_fused_variant_masks_grouped_fp16():
     x = _case(900, 128, "fp16", True, B=2, H=4, Hkv=2, seed=12)
     x["kv_lens"] = torch.tensor([900, 451], dtype=torch.int32)
     x["block_mask"] = random_tile_mask(8, 0.6, seed=5)
-    with _FusedVariant():
-        run_gpu(x, backward=False)
-        check_backward_given_o(x)
+    run_gpu(x, backward=False)
+    check_backward_given_o(x, fused=True)
 
 
-def test_backward_variant_rejects_unknown():
+def test_default_backward_is_not_changed_by_the_fused_call():
+    """The variant is chosen per call: a fused call in between leaves the default backward's
+    bits unchanged (there is no process-wide switch any more)."""
     import exact_io_aware_23_gb300 as fa
-    with pytest.raises(fa.FaError):
-        fa.set_backward_variant(7)
+    x = _case(700, 64, causal=True, B=1, H=2, seed=31)
+    q, k, v, do, kw = _dev(x)
+    o, lse = fa.forward(q, k, v, **kw)
+    first = fa.backward(q, k, v, o, lse, do, **kw)
+    fa.backward(q, k, v, o, lse, do, fused=True, **kw)
+    again = fa.backward(q, k, v, o, lse, do, **kw)
+    assert fa.check_device_status() == 0
+    assert all(torch.equal(a_, b_) for a_, b_ in zip(first, again))

@@ -9,6 +9,7 @@ import torch
 import oracle
 from oracle import dropout as odrop
 from gpu_helpers import LSE_TOL_BF16, f64
+from ideal_kernel import ideal_backward, ideal_forward
 from tolerances import assert_bf16_close, assert_lse_close
 from workloads import Workload, make_inputs
 
@@ -61,7 +62,7 @@ def test_dropout_parity(N, d, causal, p):
     assert fa.check_device_status() == 0
     qq, kk, vv, dd = (f64(x[n]) for n in ("q", "k", "v", "do"))
     O, L = oracle.forward(qq, kk, vv, x["scale"], causal=causal, dropout=drop)
-    assert_bf16_close("O", f64(o), O)
+    assert_bf16_close("O", f64(o), O, ideal=ideal_forward(x, dropout=drop))
     assert_lse_close(f64(lse), L, LSE_TOL_BF16)
     # backward on the oracle's O (rounded to bf16) and LSE, against the oracle's backward for it
     o_in = torch.from_numpy(O).to(torch.bfloat16)
@@ -70,8 +71,9 @@ def test_dropout_parity(N, d, causal, p):
     assert fa.check_device_status() == 0
     dQ, dK, dV = oracle.backward(qq, kk, vv, dd, x["scale"], causal=causal, dropout=drop,
                                  o=o_in.to(torch.float64).numpy())
-    for name, got, ref in (("dQ", dq, dQ), ("dK", dk, dK), ("dV", dv, dV)):
-        assert_bf16_close(name, f64(got), ref)
+    ideal = ideal_backward(x, dropout=drop, o=o_in)
+    for name, got, ref, idl in zip(("dQ", "dK", "dV"), (dq, dk, dv), (dQ, dK, dV), ideal):
+        assert_bf16_close(name, f64(got), ref, ideal=idl)
 
 
 def test_dropout_grouped_heads_fp16_padding():
@@ -86,15 +88,16 @@ def test_dropout_grouped_heads_fp16_padding():
     o, lse = fa.forward(q, k, v, causal=True, kv_lens=kl, dropout_p=p, seed=seed, offset=offset)
     qq, kk, vv, dd = (f64(x[n]) for n in ("q", "k", "v", "do"))
     O, L = oracle.forward(qq, kk, vv, x["scale"], causal=True, kv_lens=x["kv_lens"].numpy(), dropout=drop)
-    assert_bf16_close("O", f64(o), O)
+    assert_bf16_close("O", f64(o), O, ideal=ideal_forward(x, dropout=drop))
     o_in = torch.from_numpy(O).to(torch.float16)
     dq, dk, dv = fa.backward(q, k, v, o_in.to(dev), torch.from_numpy(L).float().to(dev), do, causal=True,
                              kv_lens=kl, dropout_p=p, seed=seed, offset=offset)
     assert fa.check_device_status() == 0
     dQ, dK, dV = oracle.backward(qq, kk, vv, dd, x["scale"], causal=True, kv_lens=x["kv_lens"].numpy(),
                                  dropout=drop, o=o_in.to(torch.float64).numpy())
-    for name, got, ref in (("dQ", dq, dQ), ("dK", dk, dK), ("dV", dv, dV)):
-        assert_bf16_close(name, f64(got), ref)
+    ideal = ideal_backward(x, dropout=drop, o=o_in)
+    for name, got, ref, idl in zip(("dQ", "dK", "dV"), (dq, dk, dv), (dQ, dK, dV), ideal):
+        assert_bf16_close(name, f64(got), ref, ideal=idl)
 
 
 def test_replay_and_offsets():
@@ -131,5 +134,6 @@ def test_dropout_long_rows():
     rows = np.sort(np.random.default_rng(1).choice(4096, 160, replace=False))
     O, L = oracle.forward(*(f64(x[n]) for n in ("q", "k", "v")), x["scale"], causal=True, rows=rows,
                           dropout=(seed, offset, _k8(p)))
-    assert_bf16_close("O", f64(o)[:, :, rows], O)
+    assert_bf16_close("O", f64(o)[:, :, rows], O,
+                      ideal=ideal_forward(x, rows=rows, dropout=(seed, offset, _k8(p))))
     assert_lse_close(f64(lse)[:, :, rows], L, LSE_TOL_BF16)

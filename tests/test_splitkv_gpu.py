@@ -7,6 +7,7 @@ import torch
 
 import oracle
 from gpu_helpers import f64
+from ideal_kernel import ideal_forward
 from tolerances import assert_bf16_close, assert_lse_close
 from workloads import WORKLOADS, Workload, make_inputs
 
@@ -27,7 +28,7 @@ def _run(x, n_splits):
 def _check(x, o, lse):
     kv = None if x["kv_lens"] is None else x["kv_lens"].numpy()
     O, L = oracle.forward(f64(x["q"]), f64(x["k"]), f64(x["v"]), x["scale"], kv_lens=kv)
-    assert_bf16_close("O", f64(o), O)
+    assert_bf16_close("O", f64(o), O, ideal=ideal_forward(x))
     assert_lse_close(f64(lse), L, LSE_TOL)
 
 
@@ -79,7 +80,8 @@ def test_decode_workload():
     kv = None
     O, L = oracle.forward(f64(x["q"]), f64(x["k"]), f64(x["v"]), x["scale"], rows=rows,
                           heads=[0, 9])
-    assert_bf16_close("O", f64(o)[:, [0, 9]][:, :, rows], O)
+    assert_bf16_close("O", f64(o)[:, [0, 9]][:, :, rows], O,
+                      ideal=ideal_forward(x, heads=[0, 9], rows=rows))
     assert_lse_close(f64(lse)[:, [0, 9]][:, :, rows], L, LSE_TOL)
 
 

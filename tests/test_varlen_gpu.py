@@ -9,6 +9,7 @@ import torch
 
 import oracle
 from gpu_helpers import LSE_TOL_BF16, f64
+from ideal_kernel import ideal_backward, ideal_forward
 from tolerances import assert_bf16_close, assert_lse_close
 from workloads import Workload, make_inputs
 
@@ -32,7 +33,8 @@ def _check(lens, H, Hkv, d, causal, dtype="bf16", seed=0):
     assert fa.check_device_status() == 0
     qq, kk, vv, dd = (f64(x[n]) for n in ("q", "k", "v", "do"))
     O, L = oracle.forward(qq, kk, vv, x["scale"], causal=causal, segments=cu)
-    assert_bf16_close("O", f64(o)[None], O)
+    xc = dict(x, causal=causal)
+    assert_bf16_close("O", f64(o)[None], O, ideal=ideal_forward(xc, segments=cu))
     assert_lse_close(f64(lse)[None], L, LSE_TOL_BF16)
     # backward on the oracle's O (rounded to the working dtype): the operator the kernel computes
     o_in = torch.from_numpy(O[0]).to(t["q"].dtype)
@@ -42,8 +44,9 @@ def _check(lens, H, Hkv, d, causal, dtype="bf16", seed=0):
     assert fa.check_device_status() == 0
     dQ, dK, dV = oracle.backward(qq, kk, vv, dd, x["scale"], causal=causal, segments=cu,
                                  o=o_in.to(torch.float64).numpy()[None])
-    for name, got, ref in (("dQ", dq, dQ), ("dK", dk, dK), ("dV", dv, dV)):
-        assert_bf16_close(name, f64(got)[None], ref)
+    ideal = ideal_backward(xc, segments=cu, o=o_in[None])
+    for name, got, ref, idl in zip(("dQ", "dK", "dV"), (dq, dk, dv), (dQ, dK, dV), ideal):
+        assert_bf16_close(name, f64(got)[None], ref, ideal=idl)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -96,7 +99,8 @@ def test_packed_long_mixture():
                                    for a, b in zip(cu[:-1], cu[1:])]))
     O, L = oracle.forward(*(f64(x[n]) for n in ("q", "k", "v")), x["scale"], causal=True,
                           segments=cu, rows=rows)
-    assert_bf16_close("O", f64(o)[None][:, :, rows], O)
+    assert_bf16_close("O", f64(o)[None][:, :, rows], O,
+                      ideal=ideal_forward(dict(x, causal=True), segments=cu, rows=rows))
     assert_lse_close(f64(lse)[None][:, :, rows], L, LSE_TOL_BF16)
 
 
