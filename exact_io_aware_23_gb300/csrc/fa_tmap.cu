@@ -41,14 +41,23 @@ void resolve_ctx() {
     g_ctx_get = reinterpret_cast<CtxGetCurrentFn>(fn);
 }
 
-// The calling thread's current CUDA context (null when none is current yet).
+// A key for the calling thread's current CUDA context: its handle, or, if the driver's
+// cuCtxGetCurrent cannot be reached, the current device (one context per device, as with the
+// runtime's primary contexts).  Null when no context is current yet.
 cudaError_t current_context(void** ctx) {
   std::call_once(g_ctx_once, resolve_ctx);
   *ctx = nullptr;
-  if (g_ctx_get == nullptr) return cudaErrorNotSupported;
-  CUcontext c = nullptr;
-  if (g_ctx_get(&c) != CUDA_SUCCESS) return cudaErrorUnknown;
-  *ctx = static_cast<void*>(c);
+  if (g_ctx_get != nullptr) {
+    CUcontext c = nullptr;
+    if (g_ctx_get(&c) == CUDA_SUCCESS) {
+      *ctx = static_cast<void*>(c);
+      return cudaSuccess;
+    }
+  }
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  *ctx = reinterpret_cast<void*>(static_cast<uintptr_t>(dev) + 1);
   return cudaSuccess;
 }
 

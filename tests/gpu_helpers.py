@@ -82,8 +82,11 @@ def compare_bwd(x, grads, heads=None, o_given=None):
     H = qq.shape[1]
     hs = list(range(H)) if heads is None else list(heads)
     og = None if o_given is None else o_given
-    dQ, dK, dV = oracle.backward(qq, kk, vv, dd, x["scale"], causal=x["causal"], kv_lens=kv,
-                                 block_mask=bm, heads=hs, o=og)
+    dQ, dK, dV, D = oracle.backward(qq, kk, vv, dd, x["scale"], causal=x["causal"], kv_lens=kv,
+                                    block_mask=bm, heads=hs, o=og, return_delta=True)
+    dmax = float(np.max(np.abs(D))) if D.size else 0.0
+    cancel = {"dQ": x["scale"] * dmax * float(np.max(np.abs(kk), initial=0.0)),
+              "dK": x["scale"] * dmax * float(np.max(np.abs(qq), initial=0.0)), "dV": 0.0}
     grouped = kk.shape[1] != H          # dK, dV then hold the key/value heads' group sums
     assert not (grouped and heads is not None)
     ideal = (None, None, None) if x["dtype"] == "fp32" else ideal_backward(x, heads=hs, o=og)
@@ -94,7 +97,7 @@ def compare_bwd(x, grads, heads=None, o_given=None):
         if x["dtype"] == "fp32":
             res[name] = assert_fp32_close(name, got, ref, FP32_MAX_ABS)
         else:
-            res[name] = assert_bf16_close(name, got, ref, ideal=idl)
+            res[name] = assert_bf16_close(name, got, ref, ideal=idl, cancel_scale=cancel[name])
     return res
 
 
