@@ -60,6 +60,10 @@ def _load() -> ctypes.CDLL:
     L.fa_version.restype = i
     L.fa_forward_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, vp]
     L.fa_forward_gqa.restype = i
+    L.fa_forward_blocksparse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, vp, sz, vp]
+    L.fa_forward_blocksparse.restype = i
+    L.fa_forward_blocksparse_workspace_size.argtypes = [i, i, i, i]
+    L.fa_forward_blocksparse_workspace_size.restype = sz
     L.fa_backward_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i,
                                   vp, vp, sz, vp]
     L.fa_backward_gqa.restype = i
@@ -148,10 +152,12 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool =
             scale: Optional[float] = None, block_mask: Optional[torch.Tensor] = None,
             kv_lens: Optional[torch.Tensor] = None, o: Optional[torch.Tensor] = None,
             lse: Optional[torch.Tensor] = None, stream=None, dropout_p: float = 0.0,
-            seed: int = 0, offset: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
+            seed: int = 0, offset: int = 0, balanced: bool = True,
+            workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """O, LSE = attention forward (fa_forward; fa_forward_gqa when k, v have fewer heads;
-    fa_forward_dropout when dropout_p > 0).  q: [B, H, N, d]; k, v: [B, Hkv, N, d]; bf16, fp16
-    or fp32 on CUDA."""
+    fa_forward_dropout when dropout_p > 0; with a block mask and 16-bit inputs,
+    fa_forward_blocksparse unless balanced=False).  q: [B, H, N, d]; k, v: [B, Hkv, N, d];
+    bf16, fp16 or fp32 on CUDA."""
     B, H, N, d, Hkv = _check_qkv(q, k, v)
     scale = 1.0 / d ** 0.5 if scale is None else float(scale)
     block_mask, kv_lens = _masks(block_mask, kv_lens, B, N, q.device)
@@ -164,6 +170,17 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool =
                                     _ptr(kv_lens), ctypes.byref(drop), _stream(stream))
         if st != FA_OK:
             raise FaError(st, "fa_forward_dropout")
+        return o, lse
+    if block_mask is not None and balanced and q.dtype != torch.float32:
+        need = int(lib.fa_forward_blocksparse_workspace_size(B, H, N, d))
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        st = lib.fa_forward_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N,
+                                        d, scale, int(bool(causal)), _ptr(block_mask),
+                                        _DTYPES[q.dtype], _ptr(kv_lens), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream))
+        if st != FA_OK:
+            raise FaError(st, "fa_forward_blocksparse")
         return o, lse
     if Hkv == H:
         st = lib.fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,

@@ -66,7 +66,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 extern "C" {
 
-int fa_version(void) { return 200; }
+int fa_version(void) { return 201; }
 
 const char* fa_status_string(fa_status s) {
   switch (s) {
@@ -109,10 +109,38 @@ fa_status make_dropout(const fa_dropout* in, fa::DropoutArgs* out) {
   return FA_OK;
 }
 
+// Balanced block-sparse forward: the caller's workspace, carved into the plan's buffers.
+struct Balance {
+  void* workspace;
+  size_t bytes;
+};
+
+constexpr int kPlanExtra = 16;                 // extra CTAs per (b, h) slice for split pairs
+constexpr int kPlanSlots = 2 * kPlanExtra;     // partial slots per slice (split ranges <= 2 x extra)
+
+// Byte offsets of the plan's buffers in the workspace: counts, plan, merge counters, partial O,
+// partial LSE (each 256-byte aligned), and the total.
+struct PlanLayout {
+  size_t counts, plan, merge, o_part, lse_part, total;
+};
+
+PlanLayout plan_layout(int B, int H, int N, int d) {
+  const size_t pairs = (size_t)(N + 255) / 256, bh = (size_t)B * H;
+  PlanLayout L;
+  L.counts = 0;
+  L.plan = round_up(pairs * sizeof(int), 256);
+  L.merge = L.plan + round_up((pairs + kPlanExtra) * 4 * sizeof(int), 256);
+  L.o_part = L.merge + round_up(bh * kPlanSlots * sizeof(int), 256);
+  L.lse_part = L.o_part + round_up(bh * kPlanSlots * 256 * (size_t)d * sizeof(float), 256);
+  L.total = L.lse_part + round_up(bh * kPlanSlots * 256 * sizeof(float), 256);
+  return L;
+}
+
 fa_status forward_impl(const void* q, const void* k, const void* v, void* o, float* lse,
                        int B, int H, int Hkv, int N, int d, float scale, int causal,
                        const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
-                       void* stream, Packing pk = {nullptr, 0}, fa::DropoutArgs drop = {}) {
+                       void* stream, Packing pk = {nullptr, 0}, fa::DropoutArgs drop = {},
+                       Balance bal = {nullptr, 0}) {
   fa_status st = check_common(B, H, N, d, scale, dtype);
   if (st != FA_OK) return st;
   st = check_heads(H, Hkv, dtype);
@@ -137,8 +165,39 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
   a.rows = pk.cu_seqlens != nullptr ? pk.total : N;
   if (pk.cu_seqlens != nullptr) a.heads_fastest = 1;     // sequences of unequal length
   a.drop = drop;
+  a.plan = nullptr;
+  a.plan_entries = 0;
+  a.n_slots = 0;
+  a.merge_count = nullptr;
   if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (bal.workspace != nullptr && block_mask != nullptr && dtype != FA_FP32) {
+    const PlanLayout L = plan_layout(B, H, N, d);
+    if (bal.bytes < L.total) return FA_ERR_INVALID_ARG;
+    char* w = static_cast<char*>(bal.workspace);
+    fa::PlanArgs p{};
+    p.block_mask = block_mask;
+    p.T = a.n_tiles;
+    p.n_pairs = (N + 255) / 256;
+    p.causal = a.causal;
+    p.extra = kPlanExtra;
+    p.n_slots = kPlanSlots;
+    p.BH = B * H;
+    int dev = 0;
+    p.sms = 152;                               // GB300's SM count when no device can be asked
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&p.sms, cudaDevAttrMultiProcessorCount, dev);
+    p.counts = reinterpret_cast<int*>(w + L.counts);
+    p.plan = reinterpret_cast<int4*>(w + L.plan);
+    p.merge_count = reinterpret_cast<int*>(w + L.merge);
+    cudaError_t e = fa::launch_blocksparse_plan(p, s);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    a.plan = p.plan;
+    a.plan_entries = p.n_pairs + kPlanExtra;
+    a.n_slots = kPlanSlots;
+    a.merge_count = p.merge_count;
+    a.o_part = reinterpret_cast<float*>(w + L.o_part);
+    a.lse_part = reinterpret_cast<float*>(w + L.lse_part);
+  }
   cudaError_t e = dtype == FA_FP32 ? fa::launch_fwd_simt(a, dtype, s) : fa::launch_fwd_sm103(a, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -161,6 +220,23 @@ fa_status fa_forward_gqa(const void* q, const void* k, const void* v, void* o, f
                          void* stream) {
   return forward_impl(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, block_mask, dtype, kv_lens,
                       stream);
+}
+
+size_t fa_forward_blocksparse_workspace_size(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
+  return plan_layout(B, H, N, d).total;
+}
+
+fa_status fa_forward_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int H, int Hkv, int N, int d, float scale, int causal,
+                                 const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (block_mask != nullptr && B > 0 && H > 0 && N > 0) {
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return FA_ERR_INVALID_ARG;
+  }
+  return forward_impl(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, block_mask, dtype, kv_lens,
+                      stream, Packing{nullptr, 0}, fa::DropoutArgs{}, Balance{workspace, workspace_bytes});
 }
 
 int fa_forward_splitkv_auto_splits(int B, int H, int Nq, int Nk) {
@@ -237,12 +313,13 @@ fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* 
 
 size_t fa_backward_workspace_size(int B, int H, int N, int d) {
   if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
-  return round_up((size_t)B * H * N * sizeof(float), 256);   // D only: no dQ accumulator
+  return fa_backward_deterministic_workspace_size(B, H, N);
 }
 
 size_t fa_backward_deterministic_workspace_size(int B, int H, int N) {
   if (B <= 0 || H <= 0 || N <= 0) return 0;
-  return round_up((size_t)B * H * N * sizeof(float), 256);   // D only: no dQ accumulator
+  // D (no dQ accumulator), then the unit order used under a tile mask (1/64 of D's size)
+  return round_up((size_t)B * H * N * sizeof(float), 256) + fa::backward_order_bytes((size_t)B * H, N);
 }
 
 size_t fa_backward_fused_workspace_size(int B, int H, int N, int d) {
@@ -293,6 +370,7 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
   fa::BwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.o = o; a.dO = dO; a.lse = lse; a.dq = dq; a.dk = dk; a.dv = dv;
   const size_t rows = (size_t)wB * H * wN;
+  a.perm = nullptr;
   if (two_pass) {                      // D only: dQ is written once, no accumulator
     a.dq_acc = nullptr;
     a.delta = static_cast<float*>(workspace);
@@ -316,6 +394,24 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
   a.drop = drop;
   if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (two_pass && block_mask != nullptr) {
+    // the units' order under the tile mask: the longest first (after D in the workspace)
+    int* w = reinterpret_cast<int*>(static_cast<char*>(workspace) + round_up(rows * sizeof(float), 256));
+    const int T = a.n_tiles;
+    fa::OrderArgs p{};
+    p.block_mask = block_mask;
+    p.T = T;
+    p.causal = a.causal;
+    p.BH = B * H;
+    p.BHkv = B * Hkv;
+    p.counts = w;
+    p.rank = p.counts + 2 * T;
+    p.order = reinterpret_cast<int2*>(p.rank + 2 * T);
+    p.order_off = reinterpret_cast<int*>(p.order + 2 * T);
+    p.perm = p.order_off + 2 * T + 1;
+    if (fa::launch_backward_order(p, s) != cudaSuccess) return FA_ERR_CUDA;
+    a.perm = p.perm;
+  }
   cudaError_t e = fa::launch_bwd_preprocess(a, dtype, s);
   if (e == cudaSuccess) {
     if (two_pass) {

@@ -29,7 +29,8 @@ bwd_split_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const BwdArgs a, const int n_kv_units, const int n_q_units) {
   (void)n_q_units;
-  const int x = (int)blockIdx.x;
+  // under a tile mask, a plan may reorder the units so that the longest start first
+  const int x = a.perm != nullptr ? a.perm[blockIdx.x] : (int)blockIdx.x;
   if (x < n_kv_units) dkdv::run<D, F16, kDrop>(x, tmQ, tmK, tmV, tmDO, a);
   else dqp::run<D, F16, kDrop>(x - n_kv_units, tmQ, tmK, tmV, tmDO, a);
 }

@@ -57,7 +57,13 @@ struct Cfg {
   static constexpr int kVec = kO + kOSlots * kTile;          // vector slot s: lse2[128], delta[128]
   static constexpr int kBar = kVec + 2 * 1024;
   static constexpr int kSmem = kBar + 256;
-  static constexpr uint32_t kDV = 0, kDK = D, kX = 2 * D, kY = 2 * D + 128;   // TMEM columns
+  // TMEM columns.  At d = 64 the accumulators leave room for a second S^T buffer, so S^T(n+1)
+  // is computed while the compute warps still work on tile n (X0/X1 alternate); at d = 128 the
+  // 512 columns hold dV, dK, one X and Y.
+  static constexpr bool kXDouble = D == 64;
+  static constexpr uint32_t kDV = 0, kDK = D, kX0 = 2 * D, kX1 = kXDouble ? 2 * D + 128 : 2 * D;
+  static constexpr uint32_t kY = kXDouble ? 2 * D + 256 : 2 * D + 128;
+  static __device__ __forceinline__ uint32_t x_col(int n) { return (n & 1) ? kX1 : kX0; }
   static constexpr uint32_t kIdescST = ptx::idesc_f32acc(128, 128, false, false, F16);  // S^T, dP^T
   static constexpr uint32_t kIdescAcc = ptx::idesc_f32acc(128, D, false, true, F16);    // dV, dK
 };
@@ -70,7 +76,7 @@ struct Bars {             // at most 256 bytes (the live-tile bitmap follows)
   uint64_t o_empty[4];
   uint64_t vec_full[2];
   uint64_t vec_empty[2];
-  uint64_t s_full;
+  uint64_t s_full[2];     // S^T(n) in TMEM: barrier n & 1, phase n >> 1
   uint64_t dp_full;
   uint64_t p_ready;
   uint64_t ds_ready;
@@ -170,7 +176,8 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
     ptx::mbar_init(ptx::smem_u32(&bars->vec_full[1]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->vec_empty[0]), 8);
     ptx::mbar_init(ptx::smem_u32(&bars->vec_empty[1]), 8);
-    ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->s_full[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->s_full[1]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->p_ready), 8);
     ptx::mbar_init(ptx::smem_u32(&bars->ds_ready), 8);
@@ -302,8 +309,8 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
         if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full[0]), 0, lim_ms, a.err);
         if (ok) {
           ptx::tc_fence_after();
-          st_mma(C::kX, sbase + C::kK, sbase + C::kQ);
-          ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+          st_mma(C::x_col(0), sbase + C::kK, sbase + C::kQ);
+          ptx::mma_commit(ptx::smem_u32(&bars->s_full[0]));
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->o_full[0]), 0, lim_ms, a.err);
         }
         if (ok) {
@@ -315,18 +322,29 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
           const int qs = n % C::kQSlots, os = n % C::kOSlots;
           const int qs1 = (n + 1) % C::kQSlots, os1 = (n + 1) % C::kOSlots;
           const bool more = n + 1 < total;
+          // S^T(n+1) into X((n+1)&1): with two X buffers it goes first, ahead of dV(n) (the
+          // buffer's last reader, dV(n-1), was issued before it); with one, behind dV(n)
+          auto next_st = [&]() -> bool {
+            if (!ptx::mbar_wait(ptx::smem_u32(&bars->q_full[qs1]), (uint32_t)((n + 1) / C::kQSlots) & 1u,
+                                lim_ms, a.err))
+              return false;
+            ptx::tc_fence_after();
+            st_mma(C::x_col(n + 1), sbase + C::kK, sbase + C::kQ + qs1 * C::kTile);
+            ptx::mma_commit(ptx::smem_u32(&bars->s_full[(n + 1) & 1]));
+            return true;
+          };
+          if (C::kXDouble && more) {
+            ok = next_st();
+            if (!ok) break;
+          }
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_ready), (uint32_t)n & 1u, lim_ms, a.err);
           if (!ok) break;
           ptx::tc_fence_after();
-          acc_mma(C::kDV, C::kX, sbase + C::kO + os * C::kTile, n == 0);
+          acc_mma(C::kDV, C::x_col(n), sbase + C::kO + os * C::kTile, n == 0);
           ptx::mma_commit(ptx::smem_u32(&bars->o_empty[os]));
-          if (more) {                                 // S^T(n+1) into X, behind dV(n)
-            ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full[qs1]), (uint32_t)((n + 1) / C::kQSlots) & 1u,
-                                lim_ms, a.err);
+          if (!C::kXDouble && more) {
+            ok = next_st();
             if (!ok) break;
-            ptx::tc_fence_after();
-            st_mma(C::kX, sbase + C::kK, sbase + C::kQ + qs1 * C::kTile);
-            ptx::mma_commit(ptx::smem_u32(&bars->s_full));
           }
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_ready), (uint32_t)n & 1u, lim_ms, a.err);
           if (!ok) break;
@@ -357,7 +375,6 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
     const float c = a.scale * kLog2e;
     const float2 c2 = make_float2(c, c);
     const bool key_ok = key < g.kv_lim;
-    const uint32_t tX = tmem + lane_off + C::kX + wg * 64;
     const uint32_t tY = tmem + lane_off + C::kY + wg * 64;
     bool ok = true;
     int n = 0;
@@ -369,9 +386,10 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
       uint64_t keep = ~0ull;
       if constexpr (kDrop) keep = keep_col64_own(a.drop, (uint32_t)(b * a.H + hk * G + hg), i * BM + wg * 64, key);
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->vec_full[vs]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
-      if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full), (uint32_t)n & 1u, lim_ms, a.err);
+      if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[n & 1]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
       if (!ok) break;
       ptx::tc_fence_after();
+      const uint32_t tX = tmem + lane_off + C::x_col(n) + wg * 64;   // S^T(n), then P^T(n)
       const float* lse2 = reinterpret_cast<const float*>(smem + C::kVec + vs * 1024) + wg * 64;
       const float* dl = lse2 + 128;
       const int kind = g.kind(i);

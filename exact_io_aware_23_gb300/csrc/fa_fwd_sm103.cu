@@ -67,6 +67,7 @@ struct Bars {            // all mbarriers of one CTA (8 bytes each)
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
   uint32_t tmem_base;
+  int merge_last;        // balanced block-sparse plan: this CTA merges its pair's ranges
 };
 
 static_assert(sizeof(Bars) <= 256, "the live-tile bitmap starts 256 bytes after the barriers");
@@ -110,7 +111,9 @@ struct Geo {
   }
 };
 
-template <int D, bool F16, bool kDrop>
+// kPlan: the balanced block-sparse variant (a work plan, split pairs, the last range merging);
+// a separate instantiation, so the others carry none of its code.
+template <int D, bool F16, bool kDrop, bool kPlan>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, FwdArgs a) {
@@ -125,18 +128,26 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   uint32_t* const live_bits = reinterpret_cast<uint32_t*>(smem + C::kBarOff + 256);
   // Each role builds its own copy after its register reallocation (cheap integer work), so no
   // value computed here has to survive, spilled, into the role loops.
-  auto make_geo = [&]() {
+  // Balanced block-sparse plan: this CTA's entry {pair, range, ranges, slot}; no work for pair < 0.
+  int4 work = make_int4(0, 0, 1, -1);
+  if constexpr (kPlan) {
+    work = a.plan[blockIdx.x / (a.B * a.H)];
+    if (work.x < 0) return;
+  }
+  // with_range: restrict [j0, j_end) to this CTA's range of live key tiles (needs the bitmap)
+  auto make_geo = [&](bool with_range) {
     // Work order.  With masks, the (b, h) slice varies fastest, so every slice's heaviest Q-tile
     // pair runs in the first waves (the last pairs when causal, the global rows of a
     // block-sparse mask).  Without, one slice's pairs run together and share its K/V stream in L2.
-    // Split-KV: the range of key tiles varies slowest.
+    // Split-KV: the range of key tiles varies slowest.  With a plan: slice fastest, then the
+    // plan's entries in order (the split ranges first).
     const int BH = a.B * a.H;
     const int n_pairs = (a.N + 2 * BM - 1) / (2 * BM);
     const int unit = blockIdx.x % (n_pairs * BH);
-    const int split = blockIdx.x / (n_pairs * BH);
-    const int bh = a.heads_fastest ? unit % BH : unit / n_pairs;
+    const int split = kPlan ? 0 : blockIdx.x / (n_pairs * BH);
+    const int bh = kPlan ? (int)(blockIdx.x % BH) : a.heads_fastest ? unit % BH : unit / n_pairs;
     const int slot = a.heads_fastest ? unit / BH : unit % n_pairs;
-    const int pair = a.causal ? n_pairs - 1 - slot : slot;
+    const int pair = kPlan ? work.x : a.causal ? n_pairs - 1 - slot : slot;
     const int b = bh / a.H, h = bh % a.H;
     Geo g;
     g.bh = bh;
@@ -167,13 +178,37 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       g.j_end = min(g.j_end, g.j0 + a.tiles_per_split);
     }
     g.bits = a.block_mask != nullptr ? live_bits : nullptr;
+    if (kPlan && with_range && work.z > 1 && g.bits != nullptr) {
+      // range r of S over this CTA's live tiles: live tiles [r c / S, (r + 1) c / S) (the last
+      // range to the end), turned into tile indices through the bitmap
+      const int words = (g.j_end + 31) / 32;
+      int c = 0;
+      for (int w = 0; w < words; ++w) c += __popc(g.bits[w]);
+      const int lo = (int)(((long long)work.y * c) / work.z);
+      const int hi = work.y == work.z - 1 ? c : (int)(((long long)(work.y + 1) * c) / work.z);
+      auto tile_of = [&](int k) {             // tile index of live tile number k (j_end if none)
+        for (int w = 0; w < words; ++w) {
+          uint32_t bits = g.bits[w];
+          const int n = __popc(bits);
+          if (k < n) {
+            for (int i = 0; i < k; ++i) bits &= bits - 1;
+            return w * 32 + __ffs(bits) - 1;
+          }
+          k -= n;
+        }
+        return g.j_end;
+      };
+      const int j_hi = hi >= c ? g.j_end : tile_of(hi);
+      g.j0 = tile_of(lo);
+      g.j_end = j_hi;
+    }
     return g;
   };
   const uint32_t lim_ms = a.dbg.wait_limit_ms;
   if (a.cu_seqlens != nullptr) {
     // Packed sequences: the grid is sized for the longest one; tiles past this sequence's end
     // have nothing to do, and offsets outside the contract are reported, not followed.
-    const Geo g0 = make_geo();
+    const Geo g0 = make_geo(false);
     if (g0.row0 < 0) {
       if (threadIdx.x == 0) atomicExch(a.err, kDevBadOffsets);
       return;
@@ -199,14 +234,12 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
     ptx::tmem_relinquish();
   }
-  if (a.block_mask != nullptr && warp == 10) {   // live-tile bitmap, one ballot per 32 tiles
-    const Geo g = make_geo();
-    {
-      for (int w = 0; w < (g.j_end + 31) / 32; ++w) {
-        const int j = w * 32 + lane;
-        const uint32_t word = __ballot_sync(0xffffffffu, j < g.j_end && g.live(j));
-        if (lane == 0) live_bits[w] = word;
-      }
+  if (a.block_mask != nullptr) {   // live-tile bitmap, one ballot per 32 tiles, words spread over all warps
+    const Geo g = make_geo(false);
+    for (int w = warp; w < (g.j_end + 31) / 32; w += kThreads / 32) {
+      const int j = w * 32 + lane;
+      const uint32_t word = __ballot_sync(0xffffffffu, j < g.j_end && g.live(j));
+      if (lane == 0) live_bits[w] = word;
     }
   }
   ptx::tc_fence_before();
@@ -216,7 +249,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
   if (warp >= 8) {
     ptx::regs_dec<88>();
-    const Geo g = make_geo();
+    const Geo g = make_geo(true);
     if (warp == 8 && lane == 0) {
       // ------------------------------- TMA producer -------------------------------------------
       ptx::tma_prefetch_desc(&tmQ);
@@ -335,7 +368,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   } else {
     // ------------------------------- softmax warpgroups -----------------------------------------
     ptx::regs_inc<200>();
-    const Geo g = make_geo();
+    const Geo g = make_geo(true);
     const int t = warp / 4;
     const int sub = warp % 4;
     const int r = sub * 32 + lane;                  // TMEM lane == row within the Q tile
@@ -459,9 +492,12 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const float inv = any ? (kDrop ? a.drop.scale : 1.f) / l_run : 0.f;
     const size_t row = (size_t)g.qs * a.rows + g.row0 + i;      // this query row on its axis
     uint16_t* orow = static_cast<uint16_t*>(a.o) + row * D;
-    // split-KV: this range's normalised partial output (fp32) and log-sum-exp
-    const size_t prow = (size_t)g.split * a.B * a.H * a.N + row;
-    float* porow = a.o_part != nullptr ? a.o_part + prow * D : nullptr;
+    // split-KV, or a split pair of a balanced plan: this range's normalised partial output (fp32)
+    // and log-sum-exp
+    const bool planned_split = kPlan && work.z > 1;
+    const size_t prow = planned_split ? ((size_t)g.bh * a.n_slots + work.w) * (2 * BM) + (i - g.q0)
+                                      : (size_t)g.split * a.B * a.H * a.N + row;
+    float* porow = (a.o_part != nullptr && (!kPlan || planned_split)) ? a.o_part + prow * D : nullptr;
 #pragma unroll 1
     for (int q4 = 0; q4 < D / 32; ++q4) {
       uint32_t o[32];
@@ -497,6 +533,64 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (porow != nullptr) a.lse_part[prow] = L;
       else a.lse[row] = L;
     }
+    if (kPlan && planned_split) {
+      // The range that finishes last merges the pair's S ranges, always in range order, with the
+      // merge law: w_r = exp(LSE_r - max LSE), O = sum w_r O_r / sum w_r, LSE = max + ln sum w_r.
+      __threadfence();                               // this range's partials, before the count
+      ptx::named_bar_sync(1, 256);                   // the eight softmax warps
+      const int first = work.w - work.y;             // the pair's first slot (its counter)
+      if (threadIdx.x == 0) {
+        const int prev = atomicAdd(a.merge_count + (size_t)g.bh * a.n_slots + first, 1);
+        bars->merge_last = prev == work.z - 1 ? 1 : 0;
+      }
+      ptx::named_bar_sync(1, 256);
+      if (bars->merge_last != 0 && i < g.N) {
+        __threadfence();
+        const size_t base = ((size_t)g.bh * a.n_slots + first) * (2 * BM) + (i - g.q0);
+        float mx = -INFINITY;
+        for (int r = 0; r < work.z; ++r) mx = fmaxf(mx, __ldcg(a.lse_part + base + (size_t)r * (2 * BM)));
+        float wsum = 0.f;
+        if (mx != -INFINITY)
+          for (int r = 0; r < work.z; ++r) {
+            const float L = __ldcg(a.lse_part + base + (size_t)r * (2 * BM));
+            wsum += L == -INFINITY ? 0.f : ptx::ex2((L - mx) * kLog2e);
+          }
+        const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll 1
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          float acc[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+          if (mx != -INFINITY)
+            for (int r = 0; r < work.z; ++r) {
+              const size_t pr = base + (size_t)r * (2 * BM);
+              const float L = __ldcg(a.lse_part + pr);
+              if (L == -INFINITY) continue;
+              const float w = ptx::ex2((L - mx) * kLog2e);
+              const float4* src = reinterpret_cast<const float4*>(a.o_part + pr * D + q4 * 32);
+#pragma unroll
+              for (int v4 = 0; v4 < 8; ++v4) {
+                const float4 x = __ldcg(src + v4);
+                acc[4 * v4 + 0] = fmaf(w, x.x, acc[4 * v4 + 0]);
+                acc[4 * v4 + 1] = fmaf(w, x.y, acc[4 * v4 + 1]);
+                acc[4 * v4 + 2] = fmaf(w, x.z, acc[4 * v4 + 2]);
+                acc[4 * v4 + 3] = fmaf(w, x.w, acc[4 * v4 + 3]);
+              }
+            }
+          uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 w;
+            w.x = ptx::pack2<F16>(acc[8 * v4 + 0] * winv, acc[8 * v4 + 1] * winv);
+            w.y = ptx::pack2<F16>(acc[8 * v4 + 2] * winv, acc[8 * v4 + 3] * winv);
+            w.z = ptx::pack2<F16>(acc[8 * v4 + 4] * winv, acc[8 * v4 + 5] * winv);
+            w.w = ptx::pack2<F16>(acc[8 * v4 + 6] * winv, acc[8 * v4 + 7] * winv);
+            dst[v4] = w;
+          }
+        }
+        a.lse[row] = wsum > 0.f ? mx + log2f(wsum) * kLn2 : -INFINITY;
+      }
+    }
   }
 
   ptx::tc_fence_before();
@@ -516,7 +610,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int D, int N, int BH, boo
                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int D, bool F16, bool kDrop>
+template <int D, bool F16, bool kDrop, bool kPlan>
 cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
   // token axis and slice count of the tensor maps: per (b, h) slice, or packed per head
@@ -526,7 +620,7 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   if ((e = make_map(&mq, a.q, D, a.rows, q_slices, F16)) != cudaSuccess) return e;
   if ((e = make_map(&mk, a.k, D, packed ? a.rows : a.Nk, kv_slices, F16)) != cudaSuccess) return e;
   if ((e = make_map(&mv, a.v, D, packed ? a.rows : a.Nk, kv_slices, F16)) != cudaSuccess) return e;
-  auto kern = fwd_sm103_kernel<D, F16, kDrop>;
+  auto kern = fwd_sm103_kernel<D, F16, kDrop, kPlan>;
   // + the live-tile bitmap of a block-sparse mask (one bit per key tile)
   const int smem = Cfg<D, F16>::kSmem + (a.block_mask != nullptr ? ((a.n_tiles + 127) / 128) * 16 : 0);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -536,7 +630,7 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   cudaFuncAttributes fattr;
   if ((e = cudaFuncGetAttributes(&fattr, kern)) != cudaSuccess) return e;
   if (fattr.numRegs * kThreads < 128 * 88 + 256 * 200) return cudaErrorInvalidConfiguration;
-  dim3 grid(((a.N + 2 * BM - 1) / (2 * BM)) * a.B * a.H * a.n_splits);
+  dim3 grid(kPlan ? a.plan_entries * a.B * a.H : ((a.N + 2 * BM - 1) / (2 * BM)) * a.B * a.H * a.n_splits);
   kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }
@@ -545,11 +639,16 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
 
 cudaError_t launch_fwd_sm103(const FwdArgs& a, fa_dtype dt, cudaStream_t s) {
   if (a.drop.enabled) {
-    if (dt == FA_FP16) return a.d == 64 ? launch<64, true, true>(a, s) : launch<128, true, true>(a, s);
-    return a.d == 64 ? launch<64, false, true>(a, s) : launch<128, false, true>(a, s);
+    if (a.plan != nullptr) return cudaErrorInvalidValue;     // no plan with dropout
+    if (dt == FA_FP16) return a.d == 64 ? launch<64, true, true, false>(a, s) : launch<128, true, true, false>(a, s);
+    return a.d == 64 ? launch<64, false, true, false>(a, s) : launch<128, false, true, false>(a, s);
   }
-  if (dt == FA_FP16) return a.d == 64 ? launch<64, true, false>(a, s) : launch<128, true, false>(a, s);
-  return a.d == 64 ? launch<64, false, false>(a, s) : launch<128, false, false>(a, s);
+  if (a.plan != nullptr) {
+    if (dt == FA_FP16) return a.d == 64 ? launch<64, true, false, true>(a, s) : launch<128, true, false, true>(a, s);
+    return a.d == 64 ? launch<64, false, false, true>(a, s) : launch<128, false, false, true>(a, s);
+  }
+  if (dt == FA_FP16) return a.d == 64 ? launch<64, true, false, false>(a, s) : launch<128, true, false, false>(a, s);
+  return a.d == 64 ? launch<64, false, false, false>(a, s) : launch<128, false, false, false>(a, s);
 }
 
 }  // namespace fa

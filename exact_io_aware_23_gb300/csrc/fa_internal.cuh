@@ -59,6 +59,28 @@ struct FwdArgs {
   const int32_t* cu_seqlens;
   int rows;
   DropoutArgs drop;
+  // Balanced block-sparse forward (fa_forward_blocksparse): a work plan maps CTA x to slice
+  // x % (B*H) and plan entry x / (B*H) = {Q-tile pair, range r, ranges S, partial slot}, pair < 0
+  // for no work.  A pair split into S > 1 ranges of its live key tiles writes fp32 partials
+  // (O_r = u_r / l_r and LSE_r) to slots [slot - r, slot - r + S) of its slice
+  // (o_part: [B*H][n_slots][256][d], lse_part: [B*H][n_slots][256]); the range that finishes last
+  // (merge_count[B*H][n_slots], counted at the first slot) merges them.  Null plan: one CTA per pair.
+  const int4* plan;
+  int plan_entries;
+  int n_slots;
+  int* merge_count;
+};
+
+// The work plan of the balanced block-sparse forward (see FwdArgs::plan).
+struct PlanArgs {
+  const uint8_t* block_mask;  // [T, T]
+  int T, n_pairs, causal;
+  int extra;                  // extra CTAs per slice (the split budget)
+  int n_slots;                // partial slots per slice (>= n_pairs' share of split ranges)
+  int BH, sms;
+  int* counts;                // [n_pairs] live key tiles of each Q-tile pair (scratch)
+  int4* plan;                 // [n_pairs + extra]
+  int* merge_count;           // [BH][n_slots], zeroed
 };
 
 struct SplitMergeArgs {       // combines the split-KV partials with the (m, l, u) merge law
@@ -96,6 +118,22 @@ struct BwdArgs {
   const int32_t* cu_seqlens;  // packed sequences, as in FwdArgs
   int rows;
   DropoutArgs drop;
+  // Order of the two-pass backward's units under a tile mask: CTA x runs the unit that CTA
+  // perm[x] runs without a plan (dK/dV units of key tile j at j*B*Hkv + slice, then dQ units).
+  // Null: that order itself.
+  const int* perm;
+};
+
+// The unit order of the two-pass backward under a tile mask (see BwdArgs::order).
+struct OrderArgs {
+  const uint8_t* block_mask;  // [T, T]
+  int T, causal;
+  int BH, BHkv;               // query slices, key/value slices
+  int* counts;                // [2T] live tiles of key tile j (first T), of query tile i (next T)
+  int* rank;                  // [2T] scratch
+  int2* order;                // [2T] scratch: {kind, tile} in launch order
+  int* order_off;             // [2T + 1] scratch: first CTA of each entry
+  int* perm;                  // [T * (BHkv + BH)]
 };
 
 // Rows of the query-side tensors (Q, O, dO, dQ, LSE, D) over all slices.
@@ -124,5 +162,18 @@ cudaError_t launch_bwd_dq_convert(const BwdArgs& a, fa_dtype dt, cudaStream_t s)
 
 // Split-KV merge: O = sum_s w_s O_s / sum_s w_s, LSE = m + ln sum_s w_s, w_s = exp(LSE_s - m).
 cudaError_t launch_splitkv_merge(const SplitMergeArgs& m, fa_dtype dt, cudaStream_t s);
+
+// Live key tiles per Q-tile pair of a tile mask, then the split plan (fa_plan.cu).
+cudaError_t launch_blocksparse_plan(const PlanArgs& p, cudaStream_t s);
+
+// Live tiles per key tile and per query tile of a tile mask, then the backward's unit order.
+cudaError_t launch_backward_order(const OrderArgs& p, cudaStream_t s);
+
+// Bytes of the backward's unit-order buffers for N keys and BH slices (a multiple of 256).
+inline size_t backward_order_bytes(size_t BH, int N) {
+  const size_t T = (size_t)(N + 127) / 128;
+  const size_t ints = 2 * T + 2 * T + 4 * T + (2 * T + 1) + 2 * T * BH;
+  return (ints * sizeof(int) + 255) / 256 * 256;
+}
 
 }  // namespace fa

@@ -83,6 +83,29 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
                      void* stream);
 
 /*
+ * fa_forward_gqa for tile masks whose query rows have very unequal numbers of live key tiles (the
+ * global rows of a local + global pattern, "FlashAttention paper story", block-sparse paragraph,
+ * attend to every key tile while the others see a few).  With one CTA per 256-row pair of query
+ * tiles such a pair is a chain of hundreds of tiles that outlasts all the other work.  Here a
+ * plan computed on the device from the mask cuts every pair whose live key tiles exceed a target
+ * length into ranges run by separate CTAs (at most 16 extra CTAs per (b, h) slice), and the range
+ * that finishes last merges the ranges' partial results with the merge law of the online-softmax
+ * statistics ("FlashAttention：让精确注意力服从内存层次", section "Online softmax").  The plan
+ * depends only on the mask: results are the same bits on every call (they can differ from
+ * fa_forward's in the last bits, the sums being grouped differently).
+ *   workspace : >= fa_forward_blocksparse_workspace_size(B, H, N, d) bytes, 256-byte aligned,
+ *               caller-owned, contents on entry irrelevant; calls in flight at once need their own
+ *               (it holds the plan and the partial results: about B*H * 32 * 256 * (d+1) * 4 bytes)
+ * Without a block mask, or with fp32 inputs, this is fa_forward_gqa (the workspace is not used).
+ * Other arguments, errors and ownership as in fa_forward_gqa.
+ */
+size_t fa_forward_blocksparse_workspace_size(int B, int H, int N, int d);
+fa_status fa_forward_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int H, int Hkv, int N, int d, float scale, int causal,
+                                 const uint8_t* block_mask, fa_dtype dtype, const int32_t* kv_lens,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Grouped-query attention (the pages list "GQA head mapping" among the semantics production use
  * needs: "FlashAttention：让精确注意力服从内存层次", list after the CPU reference): H query heads
  * share Hkv key/value heads, query head h reading key/value head h / (H / Hkv).  K and V (and, in
@@ -220,8 +243,9 @@ size_t fa_forward_splitkv_workspace_size(int B, int H, int Nq, int d, int n_spli
 int fa_forward_splitkv_auto_splits(int B, int H, int Nq, int Nk);
 
 /* Bytes of workspace fa_backward, fa_backward_gqa and fa_backward_noalloc's path need for these
- * sizes: one fp32 per query row for D (B*H*N*4, rounded up to a multiple of 256).  d is not used;
- * it is kept so that the size is asked for with the problem's own sizes. */
+ * sizes: one fp32 per query row for D (B*H*N*4), then the order of the work units used under a
+ * tile mask (2 ints per 128-row tile and slice, about 1/64 of D), each rounded up to a multiple
+ * of 256.  d is not used; it is kept so that the size is asked for with the problem's own sizes. */
 size_t fa_backward_workspace_size(int B, int H, int N, int d);
 
 /*
@@ -257,7 +281,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
  * built into the library; every GPU that loads the library holds it until the process exits.
  * Arguments and results are those of fa_backward (the same path: two-pass for bf16/fp16,
  * CUDA cores for fp32).  Returns FA_ERR_UNSUPPORTED, launching nothing, when
- * fa_backward_workspace_size(B, H, N, d) exceeds that size (more than 8 388 608 query rows
+ * fa_backward_workspace_size(B, H, N, d) exceeds that size (above about 8.2 million query rows
  * B*H*N).  The first call in a CUDA context looks up the array's device address and caches it
  * for that context; make it before any stream capture.  Not supported after cudaDeviceReset on
  * the device (the cached address can be stale).  All calls share the array: calls that overlap

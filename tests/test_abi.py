@@ -54,7 +54,7 @@ def test_status_strings(lib):
     assert lib.fa_status_string(0) == b"FA_OK"
     assert lib.fa_status_string(4) == b"FA_ERR_TIMEOUT"
     assert lib.fa_status_string(99) == b"FA_UNKNOWN_STATUS"
-    assert lib.fa_version() == 200
+    assert lib.fa_version() == 201
 
 
 P = ctypes.c_void_p(0x10000)       # aligned, never dereferenced: every call below returns early
@@ -89,9 +89,12 @@ def test_forward_argument_checks(lib):
 
 def test_backward_argument_checks(lib):
     ws = lib.fa_backward_workspace_size(2, 3, 100, 64)
-    assert ws % 256 == 0 and 2 * 3 * 100 * 4 <= ws < 2 * 3 * 100 * 4 + 256     # D only
+    # D (one fp32 per query row), then the unit order used under a tile mask (2 ints per tile and
+    # slice, plus a few per tile); no dQ accumulator
+    assert ws % 256 == 0 and 2 * 3 * 100 * 4 <= ws <= 2560 + 256
     assert lib.fa_backward_workspace_size(0, 3, 100, 64) == 0
-    assert lib.fa_backward_workspace_size(1, 16, 16384, 128) == 1 << 20   # the long workload: 1 MiB
+    big = lib.fa_backward_workspace_size(1, 16, 16384, 128)    # the long workload: about 1 MiB
+    assert (1 << 20) <= big < (1 << 20) + (1 << 15)
 
     def bwd(dq=P, workspace=P, wsb=ws, d=64, N=100, dtype=0):
         return lib.fa_backward(P, P, P, P, P, P, dq, P, P, 2, 3, N, d, 0.125, 0, None, dtype, None,
@@ -303,3 +306,23 @@ def test_splitkv_gqa_argument_checks(lib):
     assert call(dtype=1) == UNSUPPORTED
     assert call(wsb=ws - 256) == INVALID          # same workspace as the ungrouped call
     assert call(Nq=0) == OK
+
+
+def test_blocksparse_forward_argument_checks(lib):
+    """The balanced block-sparse forward needs its workspace (plan + partials) only with a mask."""
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_forward_blocksparse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, vp, sz, vp]
+    lib.fa_forward_blocksparse_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_forward_blocksparse_workspace_size.restype = sz
+    ws = lib.fa_forward_blocksparse_workspace_size(1, 8, 65536, 64)
+    # 32 partial slots of 256 rows per slice: O (d fp32) and LSE, plus the plan
+    assert ws % 256 == 0 and ws >= 8 * 32 * 256 * 65 * 4
+    assert lib.fa_forward_blocksparse_workspace_size(1, 8, 0, 64) == 0
+
+    def call(mask=P, w=P, wsb=ws, N=65536, dtype=0):
+        return lib.fa_forward_blocksparse(P, P, P, P, P, 1, 8, 8, N, 64, 0.125, 0, mask, dtype, None,
+                                          w, wsb, None)
+    assert call(w=None) == INVALID
+    assert call(w=ctypes.c_void_p(0x10010)) == INVALID      # not 256-byte aligned
+    assert call(N=786432 + 1) == UNSUPPORTED                 # the tile-mask size limit
+    assert call(N=0) == OK
