@@ -447,7 +447,7 @@ def run_ours(args, w):
                      "workspace_bytes": ws_bytes,
                      "bytes_per_q_row_element": mem_total / float(B * H * N * d),
                      "one_fp32_score_matrix_bytes": 4 * B * H * N * N},
-        "gpu_launches": LAUNCHES_PER_STEP["fused" if args.fused_backward else "two_pass"] * args.steps,
+        "gpu_launches": launches_per_step(args, x) * args.steps,
         "clocks": clocks.summary(),
     }
     if F_eff != F:
@@ -472,6 +472,17 @@ def run_ours(args, w):
 # kernels of ours launched per step: forward 1; backward 2 (preprocess, two-pass kernel) or, with
 # --fused-backward, 3 (preprocess, fused kernel, dQ convert)
 LAUNCHES_PER_STEP = {"two_pass": 3, "fused": 4}
+
+
+def launches_per_step(args, x):
+    """Our kernel launches in one forward + backward step: with a tile mask the balanced forward
+    adds its two plan kernels and the two-pass backward its two unit-order kernels."""
+    n = LAUNCHES_PER_STEP["fused" if args.fused_backward else "two_pass"]
+    if x["block_mask"] is not None and args.dropout == 0.0:
+        n += 2 + (0 if args.fused_backward else 2)
+    elif x["block_mask"] is not None and not args.fused_backward:
+        n += 2
+    return n
 
 
 def run_decode(args, w):
