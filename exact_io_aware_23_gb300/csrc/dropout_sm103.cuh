@@ -114,4 +114,33 @@ __device__ __forceinline__ uint64_t keep_col64_own(const DropoutArgs& d, uint32_
   return bits;
 }
 
+// 32-element forms of the two above (each lane on its own, 8 calls): a query over keys
+// j0 .. j0+31, a key over queries i0 .. i0+31.
+__device__ __forceinline__ uint64_t keep_row32_own(const DropoutArgs& d, uint32_t bh, int i, int j0) {
+  uint64_t bits = 0;
+  const uint32_t sel = (uint32_t)i & 3u;
+#pragma unroll 4
+  for (int g = 0; g < 8; ++g) {
+    const uint4 r = philox4x32_10((uint32_t)(j0 >> 2) + g, (uint32_t)i >> 2, bh, d.offset, d.seed_lo,
+                                  d.seed_hi);
+    const uint32_t w = sel == 0 ? r.x : sel == 1 ? r.y : sel == 2 ? r.z : r.w;
+    bits |= (uint64_t)keep4(w, (uint32_t)d.k8) << (4 * g);
+  }
+  return bits;
+}
+__device__ __forceinline__ uint64_t keep_col32_own(const DropoutArgs& d, uint32_t bh, int i0, int j) {
+  uint64_t bits = 0;
+  const uint32_t sh = 8u * ((uint32_t)j & 3u);
+  const uint32_t k8 = (uint32_t)d.k8;
+#pragma unroll 4
+  for (int g = 0; g < 8; ++g) {
+    const uint4 r = philox4x32_10((uint32_t)j >> 2, (uint32_t)(i0 >> 2) + g, bh, d.offset, d.seed_lo,
+                                  d.seed_hi);
+    const uint32_t k4 = (((r.x >> sh) & 0xFFu) < k8 ? 1u : 0u) | (((r.y >> sh) & 0xFFu) < k8 ? 2u : 0u) |
+                        (((r.z >> sh) & 0xFFu) < k8 ? 4u : 0u) | (((r.w >> sh) & 0xFFu) < k8 ? 8u : 0u);
+    bits |= (uint64_t)k4 << (4 * g);
+  }
+  return bits;
+}
+
 }  // namespace fa

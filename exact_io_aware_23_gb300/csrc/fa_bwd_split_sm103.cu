@@ -18,13 +18,11 @@
 namespace fa {
 namespace {
 
-static_assert(dkdv::kThreads == dqp::kThreads, "both passes run with the same block size");
-
-// 320 threads = 10 warps, one CTA per SM.  The warps are spread over the SM's four 16K-register
-// partitions, three on some of them, so a thread may hold at most 16384 / 96 -> 168 registers
-// (a 200-register build does not launch).
+// Both passes run with BwdLayout<D>'s block, one CTA per SM: at d = 128 320 threads (10 warps,
+// three on some of the SM's four 16K-register partitions, so at most 16384 / 96 -> 168
+// registers a thread), at d = 64 576 (18 warps, at most 112).
 template <int D, bool F16, bool kDrop>
-__global__ void __launch_bounds__(dkdv::kThreads, 1)
+__global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
 bwd_split_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const BwdArgs a, const int n_kv_units, const int n_q_units) {
@@ -67,7 +65,7 @@ cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int n_t = (a.N + 127) / 128;
   const int n_kv = n_t * BHkv, n_q = n_t * BH;
-  kern<<<dim3(n_kv + n_q), dkdv::kThreads, smem, s>>>(mq, mk, mv, mdo, a, n_kv, n_q);
+  kern<<<dim3(n_kv + n_q), BwdLayout<D>::kThreads, smem, s>>>(mq, mk, mv, mdo, a, n_kv, n_q);
   return cudaGetLastError();
 }
 

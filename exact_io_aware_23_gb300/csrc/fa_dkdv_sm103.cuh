@@ -9,20 +9,21 @@
 // dQ is left to the query-stationary kernel (fa_dq_sm103.cu), so nothing here is added from
 // several CTAs and the results do not depend on scheduling.
 //
-// GB300 design: one CTA per 128-key tile of one (b, h) key/value slice, 320 threads, visiting
-// every live query tile of every query head that reads the slice (one, or the G heads of a
-// group under grouped-query attention).  Key rows sit on the TMEM lanes: a thread owns one key.
-//   warp 8      TMA producer: K_j, V_j once; Q_i through a three-slot ring and dO_i through a
+// GB300 design: one CTA per 128-key tile of one (b, h) key/value slice, visiting every live
+// query tile of every query head that reads the slice (one, or the G heads of a group under
+// grouped-query attention).  Key rows sit on the TMEM lanes: a thread owns one key.  kWG compute
+// warpgroups (BwdLayout: four at d = 64, two at d = 128) then the two warps below.
+//   producer    TMA producer: K_j, V_j once; Q_i through a three-slot ring and dO_i through a
 //               two-slot ring (a Q tile is read until dK, a dO tile only until dV), and the
 //               tile's -LSE*log2(e) and D vectors through a two-slot ring in shared memory.
-//   warp 9      MMA issuer, one thread, in the order
+//   MMA warp    MMA issuer, one thread, in the order
 //                   dV += P^T(n) dO_n,  S^T(n+1) = K Q_{n+1}^T,  dK += dS^T(n) Q_n,
 //                   dP^T(n+1) = V dO_{n+1}^T
 //               so the tensor pipe computes the next tile's S^T while the compute warps build
 //               dS^T(n), and dK(n), dP^T(n+1) while they build P^T(n+1).
-//   warps 0-7   two warpgroups over the tile's query columns [0,64) and [64,128): P^T and dS^T
-//               in registers, packed to bf16/fp16 pairs into the first 32 columns of the
-//               warpgroup's own 64 columns of X and Y (no other warp reads those).
+//   compute     warpgroup w over the tile's query columns [w*c, (w+1)*c), c = 128 / kWG: P^T
+//               and dS^T in registers, packed to bf16/fp16 pairs into the first c/2 columns of
+//               the warpgroup's own c columns of X and Y (no other warp reads those).
 //   TMEM: dV [0,d), dK [d,2d), X = S^T / P^T [2d, 2d+128), Y = dP^T / dS^T [2d+128, 2d+256).
 #pragma once
 
@@ -41,7 +42,6 @@ namespace dkdv {
 
 constexpr int BM = 128;          // query rows per tile
 constexpr int BN = 128;          // keys per CTA
-constexpr int kThreads = 320;
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -119,6 +119,8 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
                                     const CUtensorMap& tmV, const CUtensorMap& tmDO,
                                     const BwdArgs& a) {
   using C = Cfg<D, F16>;
+  using L = BwdLayout<D>;
+  constexpr int kCols = L::kCols;                // query columns per compute warpgroup
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if ((ptx::smem_u32(smem) & 1023u) != 0) {      // the operand tiles need 1 KB alignment
@@ -174,17 +176,17 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
     }
     ptx::mbar_init(ptx::smem_u32(&bars->vec_full[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->vec_full[1]), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->vec_empty[0]), 8);
-    ptx::mbar_init(ptx::smem_u32(&bars->vec_empty[1]), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->vec_empty[0]), L::kComputeWarps);
+    ptx::mbar_init(ptx::smem_u32(&bars->vec_empty[1]), L::kComputeWarps);
     ptx::mbar_init(ptx::smem_u32(&bars->s_full[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->s_full[1]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->p_ready), 8);
-    ptx::mbar_init(ptx::smem_u32(&bars->ds_ready), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->p_ready), L::kComputeWarps);
+    ptx::mbar_init(ptx::smem_u32(&bars->ds_ready), L::kComputeWarps);
     ptx::mbar_init(ptx::smem_u32(&bars->acc_done), 1);
     ptx::fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == L::kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -192,7 +194,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
   if (a.block_mask != nullptr) {                 // live-tile bitmap, one ballot per 32 tiles
     uint32_t* live_bits = reinterpret_cast<uint32_t*>(smem + C::kBar + 256);
     g.bits = live_bits;
-    for (int w = warp; w < (g.i_end + 31) / 32; w += kThreads / 32) {
+    for (int w = warp; w < (g.i_end + 31) / 32; w += L::kThreads / 32) {
       const int i = w * 32 + lane;
       const uint32_t word = __ballot_sync(0xffffffffu, i >= g.i_begin && i < g.i_end && g.kind(i) != kNone);
       if (lane == 0) live_bits[w] = word;
@@ -206,7 +208,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
   for (int i = g.next(g.i_begin); i < g.i_end; i = g.next(i + 1)) ++n_live;
   const int total = n_live * G;                  // tiles this CTA visits
 
-  if (warp == 8) {
+  if (warp == L::kProducerWarp) {
     // ------------------------------- producer (whole warp) --------------------------------------
     if (total > 0) {
       bool ok = true;
@@ -281,7 +283,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
                          lim_ms, a.err);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == L::kMmaWarp) {
     // ------------------------------- MMA issuer -------------------------------------------------
     if (lane == 0) {
       // S^T = K Q^T into X, dP^T = V dO^T into Y (K-major operands, k-steps of 16 along d)
@@ -293,13 +295,14 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
                       ptx::sdesc_sw128(src_q + off, 16, 1024), C::kIdescST, kk > 0);
         }
       };
-      // acc (+)= A^T-tile from TMEM x B: A = P^T or dS^T packed in X or Y (queries 64w..64w+63
-      // in columns 64w..64w+31), B = dO or Q with the query index as K (MN-major, 16 queries =
-      // 2048 bytes per step)
+      // acc (+)= A^T-tile from TMEM x B: A = P^T or dS^T packed in X or Y (queries c*w ..
+      // c*w+c-1 in columns c*w .. c*w+c/2-1), B = dO or Q with the query index as K (MN-major,
+      // 16 queries = 2048 bytes per step)
       auto acc_mma = [&](uint32_t acc, uint32_t src, uint32_t sb, bool first) {
+        constexpr int kSteps = kCols / 16;           // k-steps per warpgroup's columns
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          ptx::mma_ts(tmem + acc, tmem + src + (kk / 4) * 64 + (kk % 4) * 8,
+          ptx::mma_ts(tmem + acc, tmem + src + (kk / kSteps) * kCols + (kk % kSteps) * 8,
                       ptx::sdesc_sw128(sb + kk * 2048, 128 * 128, 1024), C::kIdescAcc,
                       (!first || kk > 0) ? 1u : 0u);
       };
@@ -375,34 +378,39 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
     const float c = a.scale * kLog2e;
     const float2 c2 = make_float2(c, c);
     const bool key_ok = key < g.kv_lim;
-    const uint32_t tY = tmem + lane_off + C::kY + wg * 64;
+    const uint32_t tY = tmem + lane_off + C::kY + wg * kCols;
+    constexpr int kNR = kCols / 32;                  // 32-column TMEM loads per operand
     bool ok = true;
     int n = 0;
     for (int hg = 0; hg < G && ok; ++hg)
     for (int i = g.next(g.i_begin); i < g.i_end; i = g.next(i + 1), ++n) {
       const int vs = n & 1;
-      // dropout: this key's keep bits over the warpgroup's 64 queries (generated while the
-      // scores are still being computed); the mask slice is that of query head hk*G + hg
+      // dropout: this key's keep bits over the warpgroup's queries (generated while the scores
+      // are still being computed); the mask slice is that of query head hk*G + hg
       uint64_t keep = ~0ull;
-      if constexpr (kDrop) keep = keep_col64_own(a.drop, (uint32_t)(b * a.H + hk * G + hg), i * BM + wg * 64, key);
+      if constexpr (kDrop) {
+        const uint32_t mh = (uint32_t)(b * a.H + hk * G + hg);
+        if constexpr (kCols == 64) keep = keep_col64_own(a.drop, mh, i * BM + wg * kCols, key);
+        else keep = keep_col32_own(a.drop, mh, i * BM + wg * kCols, key);
+      }
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->vec_full[vs]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
       if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[n & 1]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
       if (!ok) break;
       ptx::tc_fence_after();
-      const uint32_t tX = tmem + lane_off + C::x_col(n) + wg * 64;   // S^T(n), then P^T(n)
-      const float* lse2 = reinterpret_cast<const float*>(smem + C::kVec + vs * 1024) + wg * 64;
+      const uint32_t tX = tmem + lane_off + C::x_col(n) + wg * kCols;   // S^T(n), then P^T(n)
+      const float* lse2 = reinterpret_cast<const float*>(smem + C::kVec + vs * 1024) + wg * kCols;
       const float* dl = lse2 + 128;
       const int kind = g.kind(i);
-      const int q0 = i * BM + wg * 64;               // first query column of this warpgroup
-      // P^T for this thread's key row over 64 query columns
-      float p[64];
+      const int q0 = i * BM + wg * kCols;            // first query column of this warpgroup
+      // P^T for this thread's key row over the warpgroup's query columns
+      float p[kCols];
       {
-        uint32_t raw[2][32];
+        uint32_t raw[kNR][32];
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) ptx::tmem_ld32(tX + hc * 32, raw[hc]);
+        for (int hc = 0; hc < kNR; ++hc) ptx::tmem_ld32(tX + hc * 32, raw[hc]);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
+        for (int hc = 0; hc < kNR; ++hc) {
           ptx::reg_fence(raw[hc]);
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {          // column pairs: packed fp32 arithmetic
@@ -421,9 +429,9 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
         }
       }
       {
-        uint32_t pk[32];
+        uint32_t pk[kCols / 2];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < kCols / 2; ++e) {
           if constexpr (kDrop) {                     // dV takes the dropped-out probabilities
             const uint32_t kb = (uint32_t)(keep >> (2 * e)) & 3u;
             pk[e] = ptx::pack2<F16>((kb & 1u) ? p[2 * e] : 0.f, (kb & 2u) ? p[2 * e + 1] : 0.f);
@@ -431,7 +439,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
             pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
           }
         }
-        ptx::tmem_st32(tX, pk);
+        ptx::tmem_st(tX, pk);
         ptx::tmem_wait_st();
       }
       ptx::tc_fence_before();
@@ -445,12 +453,12 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
         ptx::mbar_arrive(ptx::smem_u32(&bars->q_empty[(n - 1) % C::kQSlots]));
       // dS^T = P^T * (dP^T - D)
       {
-        uint32_t raw[2][32];
+        uint32_t raw[kNR][32];
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) ptx::tmem_ld32(tY + hc * 32, raw[hc]);
+        for (int hc = 0; hc < kNR; ++hc) ptx::tmem_ld32(tY + hc * 32, raw[hc]);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
+        for (int hc = 0; hc < kNR; ++hc) {
           ptx::reg_fence(raw[hc]);
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
@@ -468,10 +476,10 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
         }
       }
       {
-        uint32_t pk[32];
+        uint32_t pk[kCols / 2];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
-        ptx::tmem_st32(tY, pk);
+        for (int e = 0; e < kCols / 2; ++e) pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
+        ptx::tmem_st(tY, pk);
         ptx::tmem_wait_st();
       }
       ptx::tc_fence_before();
@@ -481,17 +489,20 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
         ptx::mbar_arrive(ptx::smem_u32(&bars->vec_empty[vs]));   // this tile's vectors are read
       }
     }
-    // ------------------------------- epilogue: dV (warpgroup 0), dK (warpgroup 1) --------------
+    // ------------------------------- epilogue: dV (first half of the warpgroups), dK (second) ---
     const bool have = ok && n > 0;
     if (have) {
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_done), 0, lim_ms, a.err);
       ptx::tc_fence_after();
     }
-    const float mult = wg == 0 ? (kDrop ? a.drop.scale : 1.f) : a.scale;
-    uint16_t* out = static_cast<uint16_t*>(wg == 0 ? a.dv : a.dk) + ((size_t)ks * a.rows + row0 + key) * D;
-    const uint32_t src = wg == 0 ? C::kDV : C::kDK;
+    constexpr int kPer = L::kWG / 2;                 // warpgroups per output, each D / kPer columns
+    const bool is_dv = wg < kPer;
+    const int c0 = (wg % kPer) * (D / kPer);
+    const float mult = is_dv ? (kDrop ? a.drop.scale : 1.f) : a.scale;
+    uint16_t* out = static_cast<uint16_t*>(is_dv ? a.dv : a.dk) + ((size_t)ks * a.rows + row0 + key) * D + c0;
+    const uint32_t src = (is_dv ? C::kDV : C::kDK) + c0;
 #pragma unroll 1
-    for (int hc = 0; hc < D / 32; ++hc) {
+    for (int hc = 0; hc < D / kPer / 32; ++hc) {
       uint32_t raw[32];
       if (have && ok) {
         ptx::tmem_ld32(tmem + lane_off + src + hc * 32, raw);
@@ -519,7 +530,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (warp == 9) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (warp == L::kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace dkdv

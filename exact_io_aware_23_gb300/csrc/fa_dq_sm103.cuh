@@ -12,19 +12,20 @@
 // ascending order, accumulating dQ in TMEM: the result is the same bits on every run.  The cost
 // is recomputing S and dP (two more products per tile pair than the fused kernel spends on dQ).
 //
-// GB300 design: one CTA per 128-row query tile of one (b, h) slice, 320 threads.
-//   warp 8      TMA producer: Q_i and dO_i once; K_j and V_j through two rings.  V_j is free
+// GB300 design: one CTA per 128-row query tile of one (b, h) slice: kWG compute warpgroups
+// (BwdLayout: four at d = 64, two at d = 128), then the two warps below.
+//   producer    TMA producer: Q_i and dO_i once; K_j and V_j through two rings.  V_j is free
 //               once dP has read it, K_j only after dQ has: the K ring is the deeper one, so the
 //               next K tile is loaded a whole tile ahead of the product that needs it.
-//   warp 9      MMA issuer: S = Q_i K_j^T into one of two S buffers (SS); dQ += dS K_{j-1}
+//   MMA warp    MMA issuer: S = Q_i K_j^T into one of two S buffers (SS); dQ += dS K_{j-1}
 //               for the previous tile (TS: dS read from TMEM, K MN-major in shared memory),
 //               then dP = dO_i V_j^T (SS).  The tensor pipe runs the next tile's S while the
 //               compute warps work on this one.
-//   warps 0-7   two warpgroups over the tile's keys [0,64) and [64,128); thread = query row =
-//               TMEM lane.  P from S (exp2 of scale*log2e*S - LSE*log2e), dS = P (dP - D)
-//               packed to bf16/fp16 pairs into the first 32 columns of the warpgroup's own
-//               64 S columns (no other warp reads them).  At the end each warpgroup converts
-//               half of dQ's columns and stores them.
+//   compute     warpgroup w over the tile's keys [w*c, (w+1)*c), c = 128 / kWG; thread = query
+//               row = TMEM lane.  P from S (exp2 of scale*log2e*S - LSE*log2e), dS = P (dP - D)
+//               packed to bf16/fp16 pairs into the first c/2 columns of the warpgroup's own c
+//               S columns (no other warp reads them).  At the end the warpgroups convert dQ's
+//               columns, 32 or more each, and store them.
 //   TMEM: dQ [0,128) (d columns used), S buffers [128,256) and [256,384), dP [384,512).
 #pragma once
 
@@ -43,7 +44,6 @@ namespace dqp {
 
 constexpr int BM = 128;          // query rows per CTA
 constexpr int BN = 128;          // keys per tile
-constexpr int kThreads = 320;
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -110,6 +110,9 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
                                     const CUtensorMap& tmV, const CUtensorMap& tmDO,
                                     const BwdArgs& a) {
   using C = Cfg<D, F16>;
+  using L = BwdLayout<D>;
+  constexpr int kCols = L::kCols;                // keys per compute warpgroup
+  constexpr int kNR = kCols / 32;                // 32-column TMEM loads per operand
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if ((ptx::smem_u32(smem) & 1023u) != 0) {      // the operand tiles need 1 KB alignment
@@ -167,11 +170,11 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
     ptx::mbar_init(ptx::smem_u32(&bars->s_full[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->s_full[1]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->ds_ready), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->ds_ready), L::kComputeWarps);
     ptx::mbar_init(ptx::smem_u32(&bars->dq_done), 1);
     ptx::fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == L::kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -179,7 +182,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
   if (a.block_mask != nullptr) {                 // live-tile bitmap, one ballot per 32 tiles
     uint32_t* live_bits = reinterpret_cast<uint32_t*>(smem + C::kBar + 256);
     g.bits = live_bits;
-    for (int w = warp; w < (g.j_end + 31) / 32; w += kThreads / 32) {
+    for (int w = warp; w < (g.j_end + 31) / 32; w += L::kThreads / 32) {
       const int j = w * 32 + lane;
       const uint32_t word = __ballot_sync(0xffffffffu, j < g.j_end && g.kind(j) != kNone);
       if (lane == 0) live_bits[w] = word;
@@ -191,7 +194,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
   const uint32_t tmem = bars->tmem_base;
   const bool any = g.next(0) < g.j_end;
 
-  if (warp == 8) {
+  if (warp == L::kProducerWarp) {
     // ------------------------------- TMA producer -----------------------------------------------
     if (lane == 0 && any) {
       bool ok = true;
@@ -228,19 +231,21 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
         ptx::mbar_wait(ptx::smem_u32(&bars->v_full[m % C::kVSlots]), (uint32_t)(m / C::kVSlots) & 1u,
                        lim_ms, a.err);
     }
-  } else if (warp == 9) {
+  } else if (warp == L::kMmaWarp) {
     // ------------------------------- MMA issuer -------------------------------------------------
     if (lane == 0) {
       bool ok = true;
       int n = 0;
-      // dQ += dS(m) K(m): A = dS packed in S buffer m&1 (keys 64w..64w+63 in its columns
-      // 64w..64w+31), B = K_m with the key index as K (MN-major, 16 keys = 2048 bytes a step)
+      // dQ += dS(m) K(m): A = dS packed in S buffer m&1 (keys c*w .. c*w+c-1 in its columns
+      // c*w .. c*w+c/2-1), B = K_m with the key index as K (MN-major, 16 keys = 2048 bytes a
+      // step)
       auto dq_mma = [&](int m) {
+        constexpr int kSteps = kCols / 16;           // k-steps per warpgroup's columns
         const uint32_t sb = C::kS + (uint32_t)(m & 1) * 128;
         const uint32_t sk = sbase + C::kK + (m % C::kKSlots) * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          ptx::mma_ts(tmem + C::kDQ, tmem + sb + (kk / 4) * 64 + (kk % 4) * 8,
+          ptx::mma_ts(tmem + C::kDQ, tmem + sb + (kk / kSteps) * kCols + (kk % kSteps) * 8,
                       ptx::sdesc_sw128(sk + kk * 2048, 128 * 128, 1024), C::kIdescDQ,
                       (m > 0 || kk > 0) ? 1u : 0u);
       };
@@ -315,23 +320,26 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
     int n = 0;
     for (int j = g.next(0); j < g.j_end; j = g.next(j + 1), ++n) {
       const int kind = g.kind(j);
-      const int k0 = j * BN + wg * 64;              // first key of this warpgroup's columns
-      const uint32_t sb = C::kS + (uint32_t)(n & 1) * 128 + wg * 64;
-      // dropout: this row's keep bits over the warpgroup's 64 keys (generated while the scores
-      // are still being computed)
+      const int k0 = j * BN + wg * kCols;           // first key of this warpgroup's columns
+      const uint32_t sb = C::kS + (uint32_t)(n & 1) * 128 + wg * kCols;
+      // dropout: this row's keep bits over the warpgroup's keys (generated while the scores are
+      // still being computed)
       uint64_t keep = ~0ull;
-      if constexpr (kDrop) keep = keep_row64_own(a.drop, (uint32_t)bh, q, k0);
+      if constexpr (kDrop) {
+        if constexpr (kCols == 64) keep = keep_row64_own(a.drop, (uint32_t)bh, q, k0);
+        else keep = keep_row32_own(a.drop, (uint32_t)bh, q, k0);
+      }
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[n & 1]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
       if (!ok) break;
       ptx::tc_fence_after();
-      float p[64];
+      float p[kCols];
       {
-        uint32_t raw[2][32];
+        uint32_t raw[kNR][32];
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) ptx::tmem_ld32(tmem + lane_off + sb + hc * 32, raw[hc]);
+        for (int hc = 0; hc < kNR; ++hc) ptx::tmem_ld32(tmem + lane_off + sb + hc * 32, raw[hc]);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
+        for (int hc = 0; hc < kNR; ++hc) {
           ptx::reg_fence(raw[hc]);
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
@@ -359,12 +367,12 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
         if (n > 0) ptx::mbar_arrive(ptx::smem_u32(&bars->k_empty[(n - 1) % C::kKSlots]));
       }
       {
-        uint32_t raw[2][32];
+        uint32_t raw[kNR][32];
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) ptx::tmem_ld32(tmem + lane_off + C::kDP + wg * 64 + hc * 32, raw[hc]);
+        for (int hc = 0; hc < kNR; ++hc) ptx::tmem_ld32(tmem + lane_off + C::kDP + wg * kCols + hc * 32, raw[hc]);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
+        for (int hc = 0; hc < kNR; ++hc) {
           ptx::reg_fence(raw[hc]);
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
@@ -382,28 +390,30 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
         }
       }
       {
-        uint32_t pk[32];
+        uint32_t pk[kCols / 2];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
-        ptx::tmem_st32(tmem + lane_off + sb, pk);
+        for (int e = 0; e < kCols / 2; ++e) pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
+        ptx::tmem_st(tmem + lane_off + sb, pk);
         ptx::tmem_wait_st();
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_ready));
     }
-    // ------------------------------- epilogue: dQ = scale * acc, this warpgroup's half of d -----
+    // ------------------------------- epilogue: dQ = scale * acc, 32 or more columns a warpgroup -
     const bool have = ok && n > 0;
     if (have) {
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->dq_done), 0, lim_ms, a.err);
       ptx::tc_fence_after();
     }
-    uint16_t* out = static_cast<uint16_t*>(a.dq) + row * D + wg * (D / 2);
+    constexpr int kOutCols = D / L::kWG < 32 ? 32 : D / L::kWG;   // at d = 64 with four, two idle
+    const int c0 = wg * kOutCols;
+    uint16_t* out = static_cast<uint16_t*>(a.dq) + row * D + c0;
 #pragma unroll 1
-    for (int hc = 0; hc < D / 64; ++hc) {
+    for (int hc = 0; hc < (c0 < D ? kOutCols / 32 : 0); ++hc) {
       uint32_t raw[32];
       if (have && ok) {
-        ptx::tmem_ld32(tmem + lane_off + C::kDQ + wg * (D / 2) + hc * 32, raw);
+        ptx::tmem_ld32(tmem + lane_off + C::kDQ + c0 + hc * 32, raw);
         ptx::tmem_wait_ld();
         ptx::reg_fence(raw);
       } else {
@@ -428,7 +438,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (warp == 9) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (warp == L::kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace dqp

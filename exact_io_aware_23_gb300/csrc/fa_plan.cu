@@ -139,34 +139,28 @@ __global__ void __launch_bounds__(kPlanThreads) blocksparse_plan_kernel(PlanArgs
 // chains start in the first wave.  Each unit computes the same numbers in any order (no result is
 // added from several CTAs), so the order changes no bit of the results.
 
-// One CTA per 32 mask rows: the rows' live-tile counts, and their share of every column's count.
+// One CTA per 8 mask rows, one warp per row: the row's live-tile count, and its share of every
+// column's count (summed in shared memory, then added to the global column counts).
 __global__ void __launch_bounds__(256) tile_count_kernel(OrderArgs p) {
   extern __shared__ int colsum[];                  // [T]
-  const int T = p.T, t = threadIdx.x;
+  const int T = p.T, t = threadIdx.x, lane = t % 32;
   for (int j = t; j < T; j += 256) colsum[j] = 0;
   __syncthreads();
-  const int r0 = blockIdx.x * 32;
-  for (int rr = 0; rr < 32 && r0 + rr < T; ++rr) {
-    const int i = r0 + rr;
+  const int i = blockIdx.x * 8 + t / 32;
+  if (i < T) {
     const uint8_t* row = p.block_mask + (size_t)i * T;
     const int jmax = p.causal ? min(T, i + 1) : T;
     int c = 0;
-    for (int j = t; j < jmax; j += 256) {
-      const int live = row[j] != 0 ? 1 : 0;
-      c += live;
-      colsum[j] += live;                           // column j is owned by one thread
+    for (int j = lane; j < jmax; j += 32) {
+      if (row[j] != 0) {
+        ++c;
+        atomicAdd(colsum + j, 1);
+      }
     }
     c = __reduce_add_sync(0xffffffffu, c);
-    __shared__ int wsum[8];
-    if (t % 32 == 0) wsum[t / 32] = c;
-    __syncthreads();
-    if (t == 0) {
-      int rc = 0;
-      for (int w = 0; w < 8; ++w) rc += wsum[w];
-      p.counts[T + i] = rc;
-    }
-    __syncthreads();
+    if (lane == 0) p.counts[T + i] = c;
   }
+  __syncthreads();
   for (int j = t; j < T; j += 256)
     if (colsum[j] != 0) atomicAdd(p.counts + j, colsum[j]);
 }
@@ -243,7 +237,7 @@ cudaError_t launch_backward_order(const OrderArgs& p, cudaStream_t s) {
     e = cudaFuncSetAttribute(tile_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  tile_count_kernel<<<(p.T + 31) / 32, 256, smem, s>>>(p);
+  tile_count_kernel<<<(p.T + 7) / 8, 256, smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   backward_order_kernel<<<1, kPlanThreads, 0, s>>>(p);

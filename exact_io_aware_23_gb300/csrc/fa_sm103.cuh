@@ -22,6 +22,21 @@ cudaError_t launch_bwd_sm103(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
 // is added from several CTAs.
 cudaError_t launch_bwd_split_sm103(const BwdArgs& a, fa_dtype dt, cudaStream_t s);
 
+// Compute layout of the two-pass backward's CTAs (both passes, one launch): kWG compute
+// warpgroups, each over 128 / kWG columns of a 128 x 128 tile, then the producer warp and the
+// MMA-issuing warp.  At d = 64 the tensor work per tile is half that of d = 128 and the compute
+// warps set the pace: four warpgroups of 32 columns hide more of their latency (same results);
+// at d = 128 two of 64 measured faster.
+template <int D>
+struct BwdLayout {
+  static constexpr int kWG = D == 64 ? 4 : 2;
+  static constexpr int kCols = 128 / kWG;
+  static constexpr int kComputeWarps = 4 * kWG;
+  static constexpr int kProducerWarp = kComputeWarps;
+  static constexpr int kMmaWarp = kComputeWarps + 1;
+  static constexpr int kThreads = 32 * (kComputeWarps + 2);
+};
+
 // Encodes a tiled TMA descriptor through the driver entry point (resolved once per process).
 cudaError_t encode_tensor_map(CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank,
                               const void* base, const cuuint64_t* dims, const cuuint64_t* strides,
