@@ -39,108 +39,98 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
   return make_uint4(c0, c1, c2, c3);
 }
 
-// Keep bits of the four bytes of one 32-bit word (bit k <-> byte k).
-__device__ __forceinline__ uint32_t keep4(uint32_t w, uint32_t k8) {
-  return ((w & 0xFFu) < k8 ? 1u : 0u) | (((w >> 8) & 0xFFu) < k8 ? 2u : 0u) |
-         (((w >> 16) & 0xFFu) < k8 ? 4u : 0u) | ((w >> 24) < k8 ? 8u : 0u);
+// ---- drop flags ----------------------------------------------------------------------------------
+// Every kernel that needs the mask reads it as flags: bit 7 of a byte set iff that element is
+// dropped (its uniform is >= k8).  A flag is applied to a packed bf16/fp16 pair or to an fp32
+// value by one byte permute that copies bit 7 over the element's bytes (the prmt "replicate the
+// sign" selector) and one and-not.
+
+struct DropTest {
+  uint32_t lo7;   // low seven bits of 256 - k8, in every byte
+  uint32_t hi;    // bit 7 of 256 - k8, in every byte
+  uint32_t all;   // every flag set when k8 == 0 (nothing is kept)
+};
+
+__device__ __forceinline__ DropTest drop_test(const DropoutArgs& d) {
+  const uint32_t K = (uint32_t)(256 - d.k8) & 0xFFu;
+  DropTest t;
+  t.lo7 = (K & 0x7Fu) * 0x01010101u;
+  t.hi = (K & 0x80u) * 0x01010101u;
+  t.all = d.k8 == 0 ? ~0u : 0u;
+  return t;
 }
 
-// The four lanes of a quad (lanes 4m .. 4m+3) own four consecutive rows (or columns) of the score
-// matrix, so one call serves all four.  Each lane computes a quarter of the calls and the quad
-// exchanges the words: a 4 x 4 transpose across the quad, lane t holding row t of the input and
-// receiving column t (element t of every lane's row; element s of the result comes from lane s).
-__device__ __forceinline__ uint4 quad_transpose(uint4 w, uint32_t t) {
-  auto pick = [&](uint32_t k) { return k == 0 ? w.x : k == 1 ? w.y : k == 2 ? w.z : w.w; };
-  const uint32_t own = pick(t);
-  const uint32_t r1 = __shfl_xor_sync(0xffffffffu, pick(t ^ 1u), 1);
-  const uint32_t r2 = __shfl_xor_sync(0xffffffffu, pick(t ^ 2u), 2);
-  const uint32_t r3 = __shfl_xor_sync(0xffffffffu, pick(t ^ 3u), 3);
-  auto from = [&](uint32_t s) {          // element t of lane s's row
-    const uint32_t k = s ^ t;
-    return k == 0 ? own : k == 1 ? r1 : k == 2 ? r2 : r3;
-  };
-  return make_uint4(from(0), from(1), from(2), from(3));
+__device__ __forceinline__ uint32_t bitsel(uint32_t a, uint32_t b, uint32_t m) { return (a & m) | (b & ~m); }
+__device__ __forceinline__ uint32_t rotl(uint32_t x, uint32_t n) { return __funnelshift_l(x, x, n); }
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
 }
 
-// Query row i over 64 consecutive keys j0 .. j0+63 (j0 a multiple of 4): bit c of the result
-// is the keep bit of key j0 + c.  The quad's lanes must own rows i0 .. i0+3 (i = i0 + lane % 4).
-__device__ __forceinline__ uint64_t keep_row64(const DropoutArgs& d, uint32_t bh, int i, int j0) {
-  const uint32_t t = (uint32_t)i & 3u;
-  uint64_t bits = 0;
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    // this lane's call: key group 4m + t; after the exchange, element s = word t (this row) of
-    // the call for key group 4m + s
-    const uint4 r = philox4x32_10((uint32_t)(j0 >> 2) + 4u * m + t, (uint32_t)i >> 2, bh, d.offset,
-                                  d.seed_lo, d.seed_hi);
-    const uint4 c = quad_transpose(r, t);
-    const uint32_t k8 = (uint32_t)d.k8;
-    bits |= (uint64_t)(keep4(c.x, k8) | (keep4(c.y, k8) << 4) | (keep4(c.z, k8) << 8) |
-                       (keep4(c.w, k8) << 12)) << (16 * m);
-  }
-  return bits;
+// Flags of a word's four uniforms (bit 7 of byte b <-> byte b; the other bits are undefined).
+// byte >= k8  <=>  byte + (256 - k8) carries out of bit 7.  The low seven bits of each byte are
+// added on their own (at most 254: nothing crosses into the next byte), which gives the carry
+// into bit 7; the carry out is the majority of it and the two operands' bit 7.
+__device__ __forceinline__ uint32_t drop_flags(uint32_t w, const DropTest& c) {
+  const uint32_t s = (w & 0x7F7F7F7Fu) + c.lo7;
+  return (w & c.hi) | (w & s) | (c.hi & s);
 }
 
-// The same bits computed by each lane on its own (16 calls per 64 elements, no exchange): in the
-// backward passes, whose warps have less slack to hide the exchange's latency, this measured
-// faster than the shared form.
-__device__ __forceinline__ uint64_t keep_row64_own(const DropoutArgs& d, uint32_t bh, int i, int j0) {
-  uint64_t bits = 0;
-  const uint32_t sel = (uint32_t)i & 3u;
-#pragma unroll 4
-  for (int g = 0; g < 16; ++g) {
-    const uint4 r = philox4x32_10((uint32_t)(j0 >> 2) + g, (uint32_t)i >> 2, bh, d.offset, d.seed_lo,
-                                  d.seed_hi);
-    const uint32_t w = sel == 0 ? r.x : sel == 1 ? r.y : sel == 2 ? r.z : r.w;
-    bits |= (uint64_t)keep4(w, (uint32_t)d.k8) << (4 * g);
-  }
-  return bits;
+// One call's sixteen flags in one word: bit 7 - r of byte b = flag of (row r of the call's 4 x 4
+// block, i.e. output word r; column b, i.e. byte b).  Bits 3..0 of each byte are undefined.
+__device__ __forceinline__ uint32_t pack_flags(const uint4& r, const DropTest& c) {
+  uint32_t x = bitsel(drop_flags(r.x, c), drop_flags(r.y, c) >> 1, 0x80808080u);
+  x = bitsel(x, drop_flags(r.z, c) >> 2, 0xC0C0C0C0u);
+  x = bitsel(x, drop_flags(r.w, c) >> 3, 0xE0E0E0E0u);
+  return x | c.all;
 }
 
-// Key j over 64 consecutive queries i0 .. i0+63 (i0 a multiple of 4): bit c of the result is
-// the keep bit of query i0 + c (each lane on its own).
-__device__ __forceinline__ uint64_t keep_col64_own(const DropoutArgs& d, uint32_t bh, int i0, int j) {
-  uint64_t bits = 0;
-  const uint32_t sh = 8u * ((uint32_t)j & 3u);
-  const uint32_t k8 = (uint32_t)d.k8;
-#pragma unroll 4
-  for (int g = 0; g < 16; ++g) {
-    const uint4 r = philox4x32_10((uint32_t)j >> 2, (uint32_t)(i0 >> 2) + g, bh, d.offset, d.seed_lo,
-                                  d.seed_hi);
-    const uint32_t k4 = (((r.x >> sh) & 0xFFu) < k8 ? 1u : 0u) | (((r.y >> sh) & 0xFFu) < k8 ? 2u : 0u) |
-                        (((r.z >> sh) & 0xFFu) < k8 ? 4u : 0u) | (((r.w >> sh) & 0xFFu) < k8 ? 8u : 0u);
-    bits |= (uint64_t)k4 << (4 * g);
-  }
-  return bits;
+// Sharing one quad's calls.  The four lanes 4q .. 4q+3 of a warp own four consecutive rows (or
+// columns) of the score matrix, the ones a call covers; lane u computes and packs the call of
+// group 4m + u along the other axis, so the quad makes four calls for 64 elements a lane instead
+// of sixteen.  The packed words are exchanged once (three shuffles) and gathered into one word
+// per lane:
+
+// Row-owning lanes (lane t holds row t of the block: the forward, the dQ pass).  Result: bit
+// 7 - k of byte b = flag of (this row, column b of group 4m + (t ^ k)).  Group u's four flags are
+// brought to bit 7 of the bytes by a left shift of u ^ t.
+__device__ __forceinline__ uint32_t gather_row_flags(uint32_t P, uint32_t t) {
+  const uint32_t r1 = __shfl_xor_sync(0xffffffffu, P, 1);
+  const uint32_t r2 = __shfl_xor_sync(0xffffffffu, P, 2);
+  const uint32_t r3 = __shfl_xor_sync(0xffffffffu, P, 3);
+  // lane t ^ k's word holds this row at bit 7 - t; rotate it to bit 7 - k
+  uint32_t g = bitsel(rotl(P, t), rotl(r1, t - 1u), 0x80808080u);
+  g = bitsel(g, rotl(r2, t - 2u), 0xC0C0C0C0u);
+  return bitsel(g, rotl(r3, t - 3u), 0xE0E0E0E0u);
 }
 
-// 32-element forms of the two above (each lane on its own, 8 calls): a query over keys
-// j0 .. j0+31, a key over queries i0 .. i0+31.
-__device__ __forceinline__ uint64_t keep_row32_own(const DropoutArgs& d, uint32_t bh, int i, int j0) {
-  uint64_t bits = 0;
-  const uint32_t sel = (uint32_t)i & 3u;
-#pragma unroll 4
-  for (int g = 0; g < 8; ++g) {
-    const uint4 r = philox4x32_10((uint32_t)(j0 >> 2) + g, (uint32_t)i >> 2, bh, d.offset, d.seed_lo,
-                                  d.seed_hi);
-    const uint32_t w = sel == 0 ? r.x : sel == 1 ? r.y : sel == 2 ? r.z : r.w;
-    bits |= (uint64_t)keep4(w, (uint32_t)d.k8) << (4 * g);
-  }
-  return bits;
+// Column-owning lanes (lane s holds column s of the block: the dK/dV pass).  Result: byte k =
+// the flags of (group 4m + (s ^ k) along the rows, this column), row r at bit 7 - r.
+__device__ __forceinline__ uint32_t gather_col_flags(uint32_t P, uint32_t s) {
+  const uint32_t r1 = __shfl_xor_sync(0xffffffffu, P, 1);
+  const uint32_t r2 = __shfl_xor_sync(0xffffffffu, P, 2);
+  const uint32_t r3 = __shfl_xor_sync(0xffffffffu, P, 3);
+  const uint32_t sel = s | ((s + 4u) << 4);       // byte s of the first word, byte s of the second
+  return prmt(prmt(P, r1, sel), prmt(r2, r3, sel), 0x5410u);
 }
-__device__ __forceinline__ uint64_t keep_col32_own(const DropoutArgs& d, uint32_t bh, int i0, int j) {
-  uint64_t bits = 0;
-  const uint32_t sh = 8u * ((uint32_t)j & 3u);
-  const uint32_t k8 = (uint32_t)d.k8;
-#pragma unroll 4
-  for (int g = 0; g < 8; ++g) {
-    const uint4 r = philox4x32_10((uint32_t)j >> 2, (uint32_t)(i0 >> 2) + g, bh, d.offset, d.seed_lo,
-                                  d.seed_hi);
-    const uint32_t k4 = (((r.x >> sh) & 0xFFu) < k8 ? 1u : 0u) | (((r.y >> sh) & 0xFFu) < k8 ? 2u : 0u) |
-                        (((r.z >> sh) & 0xFFu) < k8 ? 4u : 0u) | (((r.w >> sh) & 0xFFu) < k8 ? 8u : 0u);
-    bits |= (uint64_t)k4 << (4 * g);
-  }
-  return bits;
+
+// Masks (all ones over a dropped element) from gathered flags.
+// Row form: x = gathered word << (u ^ t) for group u; pair h = elements (2h, 2h+1) of the group.
+__device__ __forceinline__ uint32_t row_pair_mask(uint32_t x, int h) {
+  return prmt(x, 0u, h ? 0xBBAAu : 0x9988u);
+}
+// Row form, element b of the group (fp32).
+__device__ __forceinline__ uint32_t row_elem_mask(uint32_t x, int b) {
+  return prmt(x, 0u, (uint32_t)(8 | b) * 0x1111u);
+}
+// Column form, group u with k = u ^ s: rows (2h, 2h+1) of the group as a pair.
+__device__ __forceinline__ uint32_t col_pair_mask(uint32_t g, int h, uint32_t k) {
+  return prmt(g << (2 * h), g << (2 * h + 1), ((8u | k) * 0x11u) | ((12u | k) * 0x1100u));
+}
+// Column form, row r of group u (k = u ^ s), fp32.
+__device__ __forceinline__ uint32_t col_elem_mask(uint32_t g, int r, uint32_t k) {
+  return prmt(g << r, 0u, (8u | k) * 0x1111u);
 }
 
 }  // namespace fa

@@ -382,16 +382,24 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
     constexpr int kNR = kCols / 32;                  // 32-column TMEM loads per operand
     bool ok = true;
     int n = 0;
+    const uint32_t sq = (uint32_t)lane & 3u;         // this key within its 4-key dropout block
+    DropTest dtest{};
+    if constexpr (kDrop) dtest = drop_test(a.drop);
     for (int hg = 0; hg < G && ok; ++hg)
     for (int i = g.next(g.i_begin); i < g.i_end; i = g.next(i + 1), ++n) {
       const int vs = n & 1;
-      // dropout: this key's keep bits over the warpgroup's queries (generated while the scores
-      // are still being computed); the mask slice is that of query head hk*G + hg
-      uint64_t keep = ~0ull;
+      // dropout: this key's drop flags over the warpgroup's queries, 16 per word (generated
+      // while the scores are still being computed; the quad shares its calls); the mask slice is
+      // that of query head hk*G + hg
+      uint32_t flags[kCols / 16];
       if constexpr (kDrop) {
         const uint32_t mh = (uint32_t)(b * a.H + hk * G + hg);
-        if constexpr (kCols == 64) keep = keep_col64_own(a.drop, mh, i * BM + wg * kCols, key);
-        else keep = keep_col32_own(a.drop, mh, i * BM + wg * kCols, key);
+#pragma unroll
+        for (int m = 0; m < kCols / 16; ++m) {
+          const uint4 r = philox4x32_10((uint32_t)key >> 2, (uint32_t)((i * BM + wg * kCols) / 4) + 4u * m + sq,
+                                        mh, a.drop.offset, a.drop.seed_lo, a.drop.seed_hi);
+          flags[m] = gather_col_flags(pack_flags(r, dtest), sq);
+        }
       }
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->vec_full[vs]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
       if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[n & 1]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
@@ -433,8 +441,8 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
 #pragma unroll
         for (int e = 0; e < kCols / 2; ++e) {
           if constexpr (kDrop) {                     // dV takes the dropped-out probabilities
-            const uint32_t kb = (uint32_t)(keep >> (2 * e)) & 3u;
-            pk[e] = ptx::pack2<F16>((kb & 1u) ? p[2 * e] : 0.f, (kb & 2u) ? p[2 * e + 1] : 0.f);
+            const uint32_t k = (((uint32_t)e >> 1) & 3u) ^ sq;   // queries 2e, 2e+1: group e/2
+            pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]) & ~col_pair_mask(flags[e / 8], e & 1, k);
           } else {
             pk[e] = ptx::pack2<F16>(p[2 * e], p[2 * e + 1]);
           }
@@ -465,8 +473,11 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
             const int col = hc * 32 + e;
             float2 dpv = make_float2(__uint_as_float(raw[hc][e]), __uint_as_float(raw[hc][e + 1]));
             if constexpr (kDrop) {                   // dP = (dO V^T) * M * 256/k8
-              const uint32_t kb = (uint32_t)(keep >> col) & 3u;
-              dpv = make_float2((kb & 1u) ? dpv.x * a.drop.scale : 0.f, (kb & 2u) ? dpv.y * a.drop.scale : 0.f);
+              const uint32_t k = (((uint32_t)col >> 2) & 3u) ^ sq;
+              const uint32_t fw = flags[col / 16];
+              dpv.x = __uint_as_float(raw[hc][e] & ~col_elem_mask(fw, col & 3, k));
+              dpv.y = __uint_as_float(raw[hc][e + 1] & ~col_elem_mask(fw, (col & 3) + 1, k));
+              dpv = ptx::mul2(dpv, make_float2(a.drop.scale, a.drop.scale));
             }
             const float2 dd = ptx::sub2(dpv, *reinterpret_cast<const float2*>(dl + col));
             const float2 ds = ptx::mul2(make_float2(p[col], p[col + 1]), dd);

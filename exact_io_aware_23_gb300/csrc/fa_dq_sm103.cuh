@@ -318,16 +318,23 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
     const float2 dd2 = make_float2(dd, dd);
     bool ok = true;
     int n = 0;
+    const uint32_t tq = (uint32_t)lane & 3u;         // this row within its 4-row dropout block
+    DropTest dtest{};
+    if constexpr (kDrop) dtest = drop_test(a.drop);
     for (int j = g.next(0); j < g.j_end; j = g.next(j + 1), ++n) {
       const int kind = g.kind(j);
       const int k0 = j * BN + wg * kCols;           // first key of this warpgroup's columns
       const uint32_t sb = C::kS + (uint32_t)(n & 1) * 128 + wg * kCols;
-      // dropout: this row's keep bits over the warpgroup's keys (generated while the scores are
-      // still being computed)
-      uint64_t keep = ~0ull;
+      // dropout: this row's drop flags over the warpgroup's keys, 16 per word (generated while
+      // the scores are still being computed; the quad shares its calls)
+      uint32_t flags[kCols / 16];
       if constexpr (kDrop) {
-        if constexpr (kCols == 64) keep = keep_row64_own(a.drop, (uint32_t)bh, q, k0);
-        else keep = keep_row32_own(a.drop, (uint32_t)bh, q, k0);
+#pragma unroll
+        for (int m = 0; m < kCols / 16; ++m) {
+          const uint4 r = philox4x32_10((uint32_t)(k0 / 4) + 4u * m + tq, (uint32_t)q >> 2, (uint32_t)bh,
+                                        a.drop.offset, a.drop.seed_lo, a.drop.seed_hi);
+          flags[m] = gather_row_flags(pack_flags(r, dtest), tq);
+        }
       }
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[n & 1]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
       if (!ok) break;
@@ -379,8 +386,10 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
             const int col = hc * 32 + e;
             float2 dpv = make_float2(__uint_as_float(raw[hc][e]), __uint_as_float(raw[hc][e + 1]));
             if constexpr (kDrop) {                   // dP = (dO V^T) * M * 256/k8
-              const uint32_t kb = (uint32_t)(keep >> col) & 3u;
-              dpv = make_float2((kb & 1u) ? dpv.x * a.drop.scale : 0.f, (kb & 2u) ? dpv.y * a.drop.scale : 0.f);
+              const uint32_t x = flags[col / 16] << ((((uint32_t)col >> 2) & 3u) ^ tq);
+              dpv.x = __uint_as_float(raw[hc][e] & ~row_elem_mask(x, col & 3));
+              dpv.y = __uint_as_float(raw[hc][e + 1] & ~row_elem_mask(x, (col & 3) + 1));
+              dpv = ptx::mul2(dpv, make_float2(a.drop.scale, a.drop.scale));
             }
             const float2 dpd = ptx::sub2(dpv, dd2);
             const float2 ds = ptx::mul2(make_float2(p[col], p[col + 1]), dpd);

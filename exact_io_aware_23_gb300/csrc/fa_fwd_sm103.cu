@@ -382,13 +382,20 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     int idx = 0;
+    const uint32_t tq = (uint32_t)lane & 3u;       // this row within its 4-row dropout block
+    DropTest dtest{};
+    if constexpr (kDrop) dtest = drop_test(a.drop);
     for (int j = g.next(g.j0); j < g.j_end; j = g.next(j + 1), ++idx) {
-      // dropout: this row's keep bits for the tile's 128 keys (generated while the scores are
-      // still being computed)
-      uint64_t keep[2] = {~0ull, ~0ull};
+      // dropout: this row's drop flags for the tile's 128 keys, 16 per word (generated while the
+      // scores are still being computed; the quad shares its calls)
+      uint32_t flags[8];
       if constexpr (kDrop) {
-        keep[0] = keep_row64(a.drop, (uint32_t)g.bh, i, j * BN);
-        keep[1] = keep_row64(a.drop, (uint32_t)g.bh, i, j * BN + 64);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const uint4 r = philox4x32_10((uint32_t)(j * BN / 4) + 4u * m + tq, (uint32_t)i >> 2, (uint32_t)g.bh,
+                                        a.drop.offset, a.drop.seed_lo, a.drop.seed_hi);
+          flags[m] = gather_row_flags(pack_flags(r, dtest), tq);
+        }
       }
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[t]), idx & 1, lim_ms, a.err);
       if (!ok) break;
@@ -465,9 +472,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             const float2 x = ptx::fma2(make_float2(s[half * 64 + 2 * e], s[half * 64 + 2 * e + 1]), c2, nm2);
             const float2 pp = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
             ls[e & 3] = ptx::add2(ls[e & 3], pp);      // the normaliser counts every allowed key
-            if constexpr (kDrop) {
-              const uint32_t kb = (uint32_t)(keep[half] >> (2 * e)) & 3u;
-              pk[e] = ptx::pack2<F16>((kb & 1u) ? pp.x : 0.f, (kb & 2u) ? pp.y : 0.f);
+            if constexpr (kDrop) {                  // keys 4u + 2h, 4u + 2h + 1 of word half*4 + e/8
+              const uint32_t u = ((uint32_t)e >> 1) & 3u;
+              const uint32_t x = flags[half * 4 + e / 8] << (u ^ tq);
+              pk[e] = ptx::pack2<F16>(pp.x, pp.y) & ~row_pair_mask(x, e & 1);
             } else {
               pk[e] = ptx::pack2<F16>(pp.x, pp.y);
             }
