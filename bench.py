@@ -412,7 +412,9 @@ def run_ours(args, w):
     if os.path.exists(tp):
         with open(tp) as f:
             rec = json.load(f)
-        ent = rec.get(w.name, {}).get(dominant)
+        # records are per kernel variant: the dropout and fused-backward instantiations have their own
+        key = w.name + ("_dropout" if args.dropout > 0.0 else "") + ("_fused" if args.fused_backward else "")
+        ent = rec.get(key, {}).get(dominant)
         if ent and ent.get("source_hash") == kernel_source_hash():
             traffic = ent.get("bytes_per_launch")
     roof.update(kernel=f"fa_{dominant} (all launches of the call)", traffic=traffic)
