@@ -19,21 +19,20 @@
 
 namespace fa {
 
+// The key of round r is (seed low + r * 0x9E3779B9, seed high + r * 0xBB67AE85) mod 2^32; the
+// host computes the ten pairs once (DropoutArgs::rk0, rk1), so a round's key is an operand of
+// the xor instead of two additions per round and call.
 __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
-                                               uint32_t k0, uint32_t k1) {
+                                               const DropoutArgs& d) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    if (r > 0) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
     const uint64_t p0 = (uint64_t)c0 * 0xD2511F53u;
     const uint64_t p1 = (uint64_t)c2 * 0xCD9E8D57u;
     const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
     const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
-    c0 = hi1 ^ c1 ^ k0;
+    c0 = hi1 ^ c1 ^ d.rk0[r];
     c1 = lo1;
-    c2 = hi0 ^ c3 ^ k1;
+    c2 = hi0 ^ c3 ^ d.rk1[r];
     c3 = lo0;
   }
   return make_uint4(c0, c1, c2, c3);

@@ -106,6 +106,11 @@ fa_status make_dropout(const fa_dropout* in, fa::DropoutArgs* out) {
   out->offset = in->offset;
   out->k8 = (int)k8;
   out->scale = k8 > 0 ? 256.f / (float)k8 : 0.f;
+  // Philox4x32-10's key schedule: round r uses the key plus r times the two Weyl increments
+  for (int r = 0; r < 10; ++r) {
+    out->rk0[r] = out->seed_lo + (uint32_t)r * 0x9E3779B9u;
+    out->rk1[r] = out->seed_hi + (uint32_t)r * 0xBB67AE85u;
+  }
   return FA_OK;
 }
 

@@ -397,7 +397,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
 #pragma unroll
         for (int m = 0; m < kCols / 16; ++m) {
           const uint4 r = philox4x32_10((uint32_t)key >> 2, (uint32_t)((i * BM + wg * kCols) / 4) + 4u * m + sq,
-                                        mh, a.drop.offset, a.drop.seed_lo, a.drop.seed_hi);
+                                        mh, a.drop.offset, a.drop);
           flags[m] = gather_col_flags(pack_flags(r, dtest), sq);
         }
       }

@@ -332,7 +332,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
 #pragma unroll
         for (int m = 0; m < kCols / 16; ++m) {
           const uint4 r = philox4x32_10((uint32_t)(k0 / 4) + 4u * m + tq, (uint32_t)q >> 2, (uint32_t)bh,
-                                        a.drop.offset, a.drop.seed_lo, a.drop.seed_hi);
+                                        a.drop.offset, a.drop);
           flags[m] = gather_row_flags(pack_flags(r, dtest), tq);
         }
       }

@@ -393,7 +393,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
           const uint4 r = philox4x32_10((uint32_t)(j * BN / 4) + 4u * m + tq, (uint32_t)i >> 2, (uint32_t)g.bh,
-                                        a.drop.offset, a.drop.seed_lo, a.drop.seed_hi);
+                                        a.drop.offset, a.drop);
           flags[m] = gather_row_flags(pack_flags(r, dtest), tq);
         }
       }

@@ -27,6 +27,7 @@ struct DropoutArgs {
   uint32_t offset;             // Philox counter word 3
   int k8;                      // keep iff the element's 8-bit uniform is below k8 (0..256)
   float scale;                 // 256 / k8, or 0 when k8 == 0
+  uint32_t rk0[10], rk1[10];   // the generator's key in each of its ten rounds (host-computed)
 };
 
 struct FwdArgs {
