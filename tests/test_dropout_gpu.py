@@ -76,6 +76,39 @@ def test_dropout_parity(N, d, causal, p):
         assert_bf16_close(name, f64(got), ref, ideal=idl)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_keep_threshold_extremes(d):
+    """The kernels test four uniform bytes at a time against k8 (a per-byte carry, not a byte-wise
+    compare instruction): every mask bit at the thresholds where that arithmetic changes form (k8
+    = 1, 127, 128, 129, 255) equals the oracle's, seen through identity V columns as above; and
+    p = 1 (k8 = 0) drops everything: O = 0 and all three gradients are zero."""
+    import exact_io_aware_23_gb300 as fa
+    B, H, N = 1, 2, 256
+    x = _case(N, d, B=B, H=H, seed=70 + d)
+    q, k = ((0.3 * x[n].float()).to(torch.bfloat16).to("cuda") for n in ("q", "k"))
+    v = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+    v[:, :, :min(d, 128)] = torch.eye(min(d, 128), dtype=torch.bfloat16, device="cuda")[:, :d]
+    seed, offset = 99, 5
+    for k8 in (1, 127, 128, 129, 255):
+        p = 1.0 - k8 / 256.0
+        assert _k8(p) == k8
+        o, _ = fa.forward(q, k, v, dropout_p=p, seed=seed, offset=offset)
+        assert fa.check_device_status() == 0
+        got = f64(o)[:, :, :, :min(d, 128)] != 0        # column c <- key c (keys 0 .. d-1)
+        for h in range(H):
+            want = odrop.keep_mask(np.arange(N), np.arange(min(d, 128)), h, seed, offset, k8)
+            assert np.array_equal(got[0, h], want), (k8, h)
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, dropout_p=1.0, seed=seed, offset=offset)
+    o0, l0 = fa.forward(q, k, v)
+    assert torch.count_nonzero(o) == 0
+    assert torch.equal(lse, l0)                        # the statistic of the undropped scores
+    grads = fa.backward(q, k, v, o, lse, do, dropout_p=1.0, seed=seed, offset=offset)
+    assert fa.check_device_status() == 0
+    assert all(torch.count_nonzero(g) == 0 for g in grads)
+
+
 def test_dropout_grouped_heads_fp16_padding():
     import exact_io_aware_23_gb300 as fa
     x = _case(520, 128, "fp16", True, B=2, H=4, Hkv=2, seed=17)
