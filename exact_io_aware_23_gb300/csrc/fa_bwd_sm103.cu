@@ -556,7 +556,8 @@ cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
   // barriers (128 bytes) + the live-tile bitmap of a block-sparse mask (one bit per query tile)
   int smem = Cfg<D, F16>::kSmem;
   if (a.block_mask != nullptr) smem = max(smem, Cfg<D, F16>::kBar + 128 + ((a.n_tiles + 127) / 128) * 16);
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static LaunchSetup setup;
+  e = prepare_launch(setup, kern, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(((a.N + BN - 1) / BN) * BHkv);
   kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mdo, mdq, a);

@@ -61,8 +61,8 @@ cudaError_t launch(const BwdArgs& a, cudaStream_t s) {
   int smem = max(dkdv::Cfg<D, F16>::kSmem, dqp::Cfg<D, F16>::kSmem);
   smem = max(smem, dkdv::Cfg<D, F16>::kBar + 256 + bitmap);
   smem = max(smem, dqp::Cfg<D, F16>::kBar + 256 + bitmap);
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
+  static LaunchSetup setup;
+  if ((e = prepare_launch(setup, kern, smem)) != cudaSuccess) return e;
   const int n_t = (a.N + 127) / 128;
   const int n_kv = n_t * BHkv, n_q = n_t * BH;
   kern<<<dim3(n_kv + n_q), BwdLayout<D>::kThreads, smem, s>>>(mq, mk, mv, mdo, a, n_kv, n_q);

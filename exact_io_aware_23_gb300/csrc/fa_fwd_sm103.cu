@@ -631,13 +631,12 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   auto kern = fwd_sm103_kernel<D, F16, kDrop, kPlan>;
   // + the live-tile bitmap of a block-sparse mask (one bit per key tile)
   const int smem = Cfg<D, F16>::kSmem + (a.block_mask != nullptr ? ((a.n_tiles + 127) / 128) * 16 : 0);
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
   // The warp groups re-split the CTA's registers (4 warps down to 88, 8 warps up to 200 per
   // thread); that only completes if the launch holds at least that many registers.
-  cudaFuncAttributes fattr;
-  if ((e = cudaFuncGetAttributes(&fattr, kern)) != cudaSuccess) return e;
-  if (fattr.numRegs * kThreads < 128 * 88 + 256 * 200) return cudaErrorInvalidConfiguration;
+  static LaunchSetup setup;
+  int regs = 0;
+  if ((e = prepare_launch(setup, kern, smem, &regs)) != cudaSuccess) return e;
+  if (regs * kThreads < 128 * 88 + 256 * 200) return cudaErrorInvalidConfiguration;
   dim3 grid(kPlan ? a.plan_entries * a.B * a.H : ((a.N + 2 * BM - 1) / (2 * BM)) * a.B * a.H * a.n_splits);
   kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, a);
   return cudaGetLastError();

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "fa_internal.cuh"
@@ -36,6 +37,44 @@ struct BwdLayout {
   static constexpr int kMmaWarp = kComputeWarps + 1;
   static constexpr int kThreads = 32 * (kComputeWarps + 2);
 };
+
+// Per-kernel launch set-up made once per device and kept: the dynamic shared memory the kernel
+// is opted in to (raised when a launch asks for more) and its registers per thread, so that a
+// launch queries and sets nothing in the runtime once its device has seen the kernel (a short
+// call's host time is a visible part of its time).
+struct LaunchSetup {
+  static constexpr int kDevices = 64;
+  std::atomic<int> smem[kDevices] = {};
+  std::atomic<int> regs[kDevices] = {};
+};
+
+template <typename Kern>
+cudaError_t prepare_launch(LaunchSetup& c, Kern kern, int smem, int* regs = nullptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < LaunchSetup::kDevices;
+  if (!cached || c.smem[dev].load(std::memory_order_acquire) < smem) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (cached) {
+      int cur = c.smem[dev].load(std::memory_order_relaxed);
+      while (cur < smem && !c.smem[dev].compare_exchange_weak(cur, smem, std::memory_order_release)) {
+      }
+    }
+  }
+  if (regs != nullptr) {
+    int r = cached ? c.regs[dev].load(std::memory_order_acquire) : 0;
+    if (r == 0) {
+      cudaFuncAttributes fa;
+      if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+      r = fa.numRegs;
+      if (cached) c.regs[dev].store(r, std::memory_order_release);
+    }
+    *regs = r;
+  }
+  return cudaSuccess;
+}
 
 // Encodes a tiled TMA descriptor through the driver entry point (resolved once per process).
 cudaError_t encode_tensor_map(CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank,
