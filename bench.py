@@ -72,32 +72,50 @@ def forward_flops(w, B, H, N, block_mask=None):
 
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons every 200 ms while running."""
+    """Samples nvidia-smi clocks and throttle reasons every 100 ms while running.
+
+    The sampler is started before the timed region and waits (up to 3 s) for its first sample,
+    so that it is running when the region starts; `mark_start` / `mark_end` bracket the region,
+    and the summary uses the samples that arrived inside it (all of them if none did).
+    """
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index, self.rows, self.proc = index, [], None
+        self.t_start, self.t_end = None, None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.monotonic()
+            while not self.rows and time.monotonic() - t0 < 3.0 and self.proc.poll() is None:
+                time.sleep(0.01)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.rows.append([x.strip() for x in line.split(",")])
+            self.rows.append((time.monotonic(), [x.strip() for x in line.split(",")]))
+
+    def mark_start(self):
+        self.t_start = time.monotonic()
+
+    def mark_end(self):
+        self.t_end = time.monotonic()
 
     def __exit__(self, *exc):
+        if self.t_end is None:
+            self.mark_end()
         if self.proc is not None:
+            time.sleep(0.15)                 # the sample that covers the region's last moments
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -108,14 +126,22 @@ class ClockSampler:
     def summary(self):
         if not self.rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        rows = [r for t, r in self.rows
+                if self.t_start is not None and self.t_start <= t <= (self.t_end or t) + 0.15]
+        inside = bool(rows)
+        if not inside:
+            rows = [r for _, r in self.rows]
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:8]) if v == "Active"})
-        pw = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "power_w_max": max(pw) if pw else None, "samples": len(self.rows)}
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v == "Active"})
+        pw = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+               "power_w_max": max(pw) if pw else None, "samples": len(rows)}
+        if not inside:
+            out["note"] = "no sample arrived inside the timed region; all samples summarised"
+        return out
 
 
 def cpu_oracle_sample(x, w, rows_per_head, heads=(0,)):
@@ -295,6 +321,7 @@ def run_ours(args, w):
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        clocks.mark_start()
         if flush:
             # hold the stream while every step is queued, so no step waits for the host
             torch.cuda._sleep(int(2e8))
@@ -309,6 +336,7 @@ def run_ours(args, w):
             ev[i][2].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
+        clocks.mark_end()
     barrier()
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
@@ -514,11 +542,13 @@ def run_decode(args, w):
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     with ClockSampler(0) as clocks:
+        clocks.mark_start()
         s0.record(stream)
         for _ in range(args.steps):
             step()
         s1.record(stream)
         torch.cuda.synchronize()
+        clocks.mark_end()
     ms = s0.elapsed_time(s1) / args.steps
     if fa.check_device_status() != 0:
         raise RuntimeError("device error during the timed region")
@@ -588,6 +618,7 @@ def run_varlen(args, w):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     torch.cuda.synchronize()
     with ClockSampler(0) as clocks:
+        clocks.mark_start()
         for i in range(args.steps):
             ev[i][0].record(stream)
             o, lse = fwd()
@@ -595,8 +626,32 @@ def run_varlen(args, w):
             fa.backward_varlen(q, k, v, o, lse, do, cu, maxl, **kw)
             ev[i][2].record(stream)
         torch.cuda.synchronize()
+        clocks.mark_end()
     if fa.check_device_status() != 0:
         raise RuntimeError("device error during the timed region")
+    # End to end, the legs in sequence: each step copies q, k, v, dO from pinned host memory,
+    # runs forward + backward through the public API and copies O, LSE, dQ, dK, dV back.
+    hin = [x[n].pin_memory() for n in ("q", "k", "v", "do")]
+    grads = fa.backward_varlen(q, k, v, o, lse, do, cu, maxl, **kw)
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse) + tuple(grads)]
+
+    def e2e_step():
+        for dst, src in zip((q, k, v, do), hin):
+            dst.copy_(src, non_blocking=True)
+        o_, lse_ = fwd()
+        g_ = fa.backward_varlen(q, k, v, o_, lse_, do, cu, maxl, **kw)
+        for dst, src in zip(hout, (o_, lse_) + tuple(g_)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
     t_fwd = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
     t_bwd = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
     F = sum(4.0 * H * n * n * d for n in w.seq_lens) * (0.5 if w.causal else 1.0)
@@ -613,6 +668,10 @@ def run_varlen(args, w):
             "roofline": {"bound": "tensor", "kernel": "fa_backward_varlen (all launches of the call)",
                          "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
                          "traffic": None, "peak_source": f"bf16_tflops of {src}"},
+            "e2e": {"value": 2.5 * F / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
+                    "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
+                    "pipelined": "no: copies in, compute and copies out in sequence on one stream"},
             "gpu_launches": 3 * args.steps, "clocks": clocks.summary()}
     print(json.dumps(line), flush=True)
 

@@ -56,11 +56,19 @@ def test_clock_summary_reads_reasons():
     reasons were active in any sample (the fields nvidia-smi prints, in the order queried)."""
     import bench
     cs = bench.ClockSampler(0)
-    cs.rows = [["2070", "2070", "300.5", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"],
-               ["2055", "2070", "950.1", "0x4", "Not Active", "Not Active", "Not Active", "Active"],
-               ["2040", "2070", "1380.0", "0x4", "Not Active", "Not Active", "Not Active", "Active"]]
+    idle = ["1200", "2070", "90.0", "0x1", "Not Active", "Not Active", "Not Active", "Not Active"]
+    cs.rows = [(0.5, idle),
+               (1.1, ["2070", "2070", "300.5", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"]),
+               (1.2, ["2055", "2070", "950.1", "0x4", "Not Active", "Not Active", "Not Active", "Active"]),
+               (1.3, ["2040", "2070", "1380.0", "0x4", "Not Active", "Not Active", "Not Active", "Active"]),
+               (2.0, idle)]
+    cs.t_start, cs.t_end = 1.0, 1.35           # only the samples inside the timed region count
     sm = cs.summary()
     assert sm["sm_mhz"] == 2055.0 and sm["sm_max_mhz"] == 2070.0
     assert sm["reasons"] == ["sw_power_cap"] and sm["power_w_max"] == 1380.0 and sm["samples"] == 3
+    assert "note" not in sm
+    cs.t_start, cs.t_end = 3.0, 3.1            # none inside: all samples, said so
+    sm = cs.summary()
+    assert sm["samples"] == 5 and "note" in sm
     cs.rows = []
     assert cs.summary()["reasons"] == ["nvidia-smi unavailable"]
