@@ -332,13 +332,13 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     for (int i = g.next(g.i_begin); i < g.i_end; i = g.next(i + 1), ++n) {
       const int bhq = bhq0 + hg;
       const int st = n & 1;
+      const int kind = g.kind(i);                    // (a read of the mask: before the waits)
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->st_full[st]), (n >> 1) & 1, lim_ms, a.err);
       if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full), n & 1, lim_ms, a.err);
       if (!ok) break;
       ptx::tc_fence_after();
       const float* lse2 = reinterpret_cast<const float*>(smem + C::kVec + st * 1024) + wg * 64;
       const float* dl = lse2 + 128;
-      const int kind = g.kind(i);
       const int q0 = i * BM + wg * 64;               // first query column of this warpgroup
       // P^T for this thread's key row over 64 query columns
       float p[64];

@@ -401,6 +401,7 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
           flags[m] = gather_col_flags(pack_flags(r, dtest), sq);
         }
       }
+      const int kind = g.kind(i);                    // (a read of the mask: before the waits)
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->vec_full[vs]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
       if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_full[n & 1]), (uint32_t)(n >> 1) & 1u, lim_ms, a.err);
       if (!ok) break;
@@ -408,7 +409,6 @@ __device__ __forceinline__ void run(const int unit, const CUtensorMap& tmQ, cons
       const uint32_t tX = tmem + lane_off + C::x_col(n) + wg * kCols;   // S^T(n), then P^T(n)
       const float* lse2 = reinterpret_cast<const float*>(smem + C::kVec + vs * 1024) + wg * kCols;
       const float* dl = lse2 + 128;
-      const int kind = g.kind(i);
       const int q0 = i * BM + wg * kCols;            // first query column of this warpgroup
       // P^T for this thread's key row over the warpgroup's query columns
       float p[kCols];

@@ -386,6 +386,9 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     DropTest dtest{};
     if constexpr (kDrop) dtest = drop_test(a.drop);
     for (int j = g.next(g.j0); j < g.j_end; j = g.next(j + 1), ++idx) {
+      // how this Q tile treats key tile j (under a tile mask a read of the mask: issued before the
+      // wait for S, so its latency does not delay the loads of S)
+      const int kind = g.kind(t, j);
       // dropout: this row's drop flags for the tile's 128 keys, 16 per word (generated while the
       // scores are still being computed; the quad shares its calls)
       uint32_t flags[8];
@@ -406,7 +409,6 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         ptx::mbar_arrive(ptx::smem_u32(&bars->kv_empty[idx % C::kKSlots]));
         if (idx > 0) ptx::mbar_arrive(ptx::smem_u32(&bars->kv_empty[C::kKSlots + (idx - 1) % C::kVSlots]));
       }
-      const int kind = g.kind(t, j);
       uint32_t pk[32];
       if (kind == kNone) {
 #pragma unroll
