@@ -123,21 +123,27 @@ struct Balance {
 constexpr int kPlanExtra = 16;                 // extra CTAs per (b, h) slice for split pairs
 constexpr int kPlanSlots = 2 * kPlanExtra;     // partial slots per slice (split ranges <= 2 x extra)
 
-// Byte offsets of the plan's buffers in the workspace: counts, plan, merge counters, partial O,
-// partial LSE (each 256-byte aligned), and the total.
+// Byte offsets of the plan's buffers in the workspace: counts, plan, merge counters (and the
+// persistent forward's unit counter after them), partial O, partial LSE, the pairs' live-tile
+// bitmaps (each 256-byte aligned), and the total.
 struct PlanLayout {
-  size_t counts, plan, merge, o_part, lse_part, total;
+  size_t counts, plan, merge, next_unit, o_part, lse_part, bits, total;
+  int words;
 };
 
 PlanLayout plan_layout(int B, int H, int N, int d) {
   const size_t pairs = (size_t)(N + 255) / 256, bh = (size_t)B * H;
+  const int T = (N + fa::kMaskTile - 1) / fa::kMaskTile;
   PlanLayout L;
+  L.words = (T + 31) / 32;
   L.counts = 0;
   L.plan = round_up(pairs * sizeof(int), 256);
   L.merge = L.plan + round_up((pairs + kPlanExtra) * 4 * sizeof(int), 256);
-  L.o_part = L.merge + round_up(bh * kPlanSlots * sizeof(int), 256);
+  L.next_unit = L.merge + bh * kPlanSlots * sizeof(int);
+  L.o_part = L.merge + round_up(bh * kPlanSlots * sizeof(int) + sizeof(int), 256);
   L.lse_part = L.o_part + round_up(bh * kPlanSlots * 256 * (size_t)d * sizeof(float), 256);
-  L.total = L.lse_part + round_up(bh * kPlanSlots * 256 * sizeof(float), 256);
+  L.bits = L.lse_part + round_up(bh * kPlanSlots * 256 * sizeof(float), 256);
+  L.total = L.bits + round_up(pairs * (size_t)L.words * sizeof(uint32_t), 256);
   return L;
 }
 
@@ -174,6 +180,9 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
   a.plan_entries = 0;
   a.n_slots = 0;
   a.merge_count = nullptr;
+  a.next_unit = nullptr;
+  a.pair_bits = nullptr;
+  a.bit_words = 0;
   if (device_error_word(&a.err) != FA_OK) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (bal.workspace != nullptr && block_mask != nullptr && dtype != FA_FP32) {
@@ -194,12 +203,18 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
     p.counts = reinterpret_cast<int*>(w + L.counts);
     p.plan = reinterpret_cast<int4*>(w + L.plan);
     p.merge_count = reinterpret_cast<int*>(w + L.merge);
+    p.pair_bits = reinterpret_cast<uint32_t*>(w + L.bits);
+    p.words = L.words;
+    p.next_unit = reinterpret_cast<int*>(w + L.next_unit);
     cudaError_t e = fa::launch_blocksparse_plan(p, s);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     a.plan = p.plan;
     a.plan_entries = p.n_pairs + kPlanExtra;
     a.n_slots = kPlanSlots;
     a.merge_count = p.merge_count;
+    a.next_unit = p.next_unit;
+    a.pair_bits = p.pair_bits;
+    a.bit_words = p.words;
     a.o_part = reinterpret_cast<float*>(w + L.o_part);
     a.lse_part = reinterpret_cast<float*>(w + L.lse_part);
   }

@@ -70,6 +70,12 @@ struct FwdArgs {
   int plan_entries;
   int n_slots;
   int* merge_count;
+  // Persistent balanced forward (d = 64): one CTA per SM claims the plan's units (entry x slice,
+  // in plan order) from next_unit, zeroed by the plan; pair_bits[pair][bit_words] are the
+  // pairs' live key tiles.  Null next_unit: one CTA per unit.
+  int* next_unit;
+  const uint32_t* pair_bits;
+  int bit_words;
 };
 
 // The work plan of the balanced block-sparse forward (see FwdArgs::plan).
@@ -82,6 +88,9 @@ struct PlanArgs {
   int* counts;                // [n_pairs] live key tiles of each Q-tile pair (scratch)
   int4* plan;                 // [n_pairs + extra]
   int* merge_count;           // [BH][n_slots], zeroed
+  uint32_t* pair_bits;        // [n_pairs][words]: bit j of a pair's row = key tile j is live
+  int words;                  // (T + 31) / 32
+  int* next_unit;             // zeroed: the persistent forward's unit counter
 };
 
 struct SplitMergeArgs {       // combines the split-KV partials with the (m, l, u) merge law

@@ -11,7 +11,8 @@
 // reproducible to the bit.
 //
 // Two launches: one warp per pair counts the pair's live key tiles (either row of the pair live,
-// causal tiles past the diagonal excluded), then one CTA turns the counts into the plan:
+// causal tiles past the diagonal excluded) and keeps them as a bitmap, then one CTA turns the
+// counts into the plan:
 //   target length  L = max(32, (live tiles of all slices / SMs) / 4)
 //   ranges         S_p = ceil(c_p / L) when c_p > L (at most 32), else 1; pairs are split in
 //                  order while their extra CTAs (S_p - 1) fit the budget, the rest run whole
@@ -36,9 +37,16 @@ __global__ void __launch_bounds__(256) pair_count_kernel(PlanArgs p) {
   const int jmax = p.causal ? min(p.T, r1 + 1) : p.T;
   const uint8_t* m0 = p.block_mask + (size_t)r0 * p.T;
   const uint8_t* m1 = r1 < p.T ? p.block_mask + (size_t)r1 * p.T : nullptr;
+  // one ballot per 32 key tiles: the pair's live-tile bitmap (kept for the persistent forward)
+  // and its count
   int c = 0;
-  for (int j = lane; j < jmax; j += 32) c += (m0[j] != 0 || (m1 != nullptr && m1[j] != 0)) ? 1 : 0;
-  c = __reduce_add_sync(0xffffffffu, c);
+  for (int w = 0; w < p.words; ++w) {
+    const int j = w * 32 + lane;
+    const bool live = j < jmax && (m0[j] != 0 || (m1 != nullptr && m1[j] != 0));
+    const uint32_t bits = __ballot_sync(0xffffffffu, live);
+    c += __popc(bits);
+    if (lane == 0) p.pair_bits[(size_t)pair * p.words + w] = bits;
+  }
   if (lane == 0) p.counts[pair] = c;
 }
 
@@ -127,6 +135,7 @@ __global__ void __launch_bounds__(kPlanThreads) blocksparse_plan_kernel(PlanArgs
   }
   for (int e = n_split + n_whole + t; e < P + p.extra; e += kPlanThreads) p.plan[e] = make_int4(-1, 0, 0, 0);
   for (int e = t; e < p.BH * p.n_slots; e += kPlanThreads) p.merge_count[e] = 0;
+  if (t == 0) *p.next_unit = 0;
 }
 
 // ---- the backward's unit order ----------------------------------------------------------------

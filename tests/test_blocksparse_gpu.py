@@ -32,8 +32,9 @@ def test_balanced_forward_against_oracle(d, causal):
     compare(x, run_gpu(x))
 
 
-def test_balanced_forward_padding_grouped_fp16():
-    x = _case(6000, 128, "fp16", causal=True, B=2, H=4, Hkv=2, seed=9, pad=(1, 6000), global_rows=3)
+@pytest.mark.parametrize("d", [64, 128])
+def test_balanced_forward_padding_grouped_fp16(d):
+    x = _case(6000, d, "fp16", causal=True, B=2, H=4, Hkv=2, seed=9, pad=(1, 6000), global_rows=3)
     x["kv_lens"] = torch.tensor([6000, 2100], dtype=torch.int32)
     compare_fwd(x, run_gpu(x, backward=False))
 
@@ -41,6 +42,24 @@ def test_balanced_forward_padding_grouped_fp16():
 def test_balanced_forward_is_reproducible_and_close_to_unbalanced():
     import exact_io_aware_23_gb300 as fa
     x = _case(16384, 64, seed=5, global_rows=4)
+    dev = torch.device("cuda:0")
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    bm = x["block_mask"].to(dev)
+    o1, l1 = fa.forward(q, k, v, block_mask=bm)
+    o2, l2 = fa.forward(q, k, v, block_mask=bm)
+    o0, l0 = fa.forward(q, k, v, block_mask=bm, balanced=False)
+    assert fa.check_device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert_bf16_close("O", f64(o1), f64(o0))
+    assert np.max(np.abs(f64(l1) - f64(l0))) <= 1e-4
+
+
+def test_balanced_forward_many_units_per_cta():
+    """At d = 64 the balanced forward is persistent (one CTA per SM claiming units from the plan):
+    with about ten units per CTA its unit entries, Q buffers and rings wrap many times.  The
+    result is reproducible and matches the unbalanced forward."""
+    import exact_io_aware_23_gb300 as fa
+    x = _case(8192, 64, B=4, H=8, seed=11, global_rows=3)
     dev = torch.device("cuda:0")
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     bm = x["block_mask"].to(dev)
