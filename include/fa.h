@@ -95,7 +95,9 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
  * fa_forward's in the last bits, the sums being grouped differently).
  *   workspace : >= fa_forward_blocksparse_workspace_size(B, H, N, d) bytes, 256-byte aligned,
  *               caller-owned, contents on entry irrelevant; calls in flight at once need their own
- *               (it holds the plan and the partial results: about B*H * 32 * 256 * (d+1) * 4 bytes)
+ *               (it holds the plan, the pairs' live-tile bitmaps, the counter from which the
+ *               d = 64 kernel's persistent CTAs claim their work, and the partial results: about
+ *               B*H * 32 * 256 * (d+1) * 4 bytes)
  * Without a block mask, or with fp32 inputs, this is fa_forward_gqa (the workspace is not used).
  * Other arguments, errors and ownership as in fa_forward_gqa.
  */
