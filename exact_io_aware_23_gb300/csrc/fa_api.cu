@@ -197,9 +197,9 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
     p.extra = kPlanExtra;
     p.n_slots = kPlanSlots;
     p.BH = B * H;
-    int dev = 0;
     p.sms = 152;                               // GB300's SM count when no device can be asked
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&p.sms, cudaDevAttrMultiProcessorCount, dev);
+    int sms = 0;
+    if (fa::sm_count(&sms) == cudaSuccess && sms > 0) p.sms = sms;
     p.counts = reinterpret_cast<int*>(w + L.counts);
     p.plan = reinterpret_cast<int4*>(w + L.plan);
     p.merge_count = reinterpret_cast<int*>(w + L.merge);
@@ -261,8 +261,9 @@ fa_status fa_forward_blocksparse(const void* q, const void* k, const void* v, vo
 
 int fa_forward_splitkv_auto_splits(int B, int H, int Nq, int Nk) {
   if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return 1;
-  int dev = 0, sms = 152;                   // GB300's SM count when no device can be asked
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 152;                            // GB300's SM count when no device can be asked
+  int n = 0;
+  if (fa::sm_count(&n) == cudaSuccess && n > 0) sms = n;
   const long long units = (long long)B * H * ((Nq + 255) / 256);   // CTAs without splitting
   const int kv_tiles = (Nk + 127) / 128;
   long long want = (2LL * sms + units - 1) / units;                 // about two CTAs per SM

@@ -135,17 +135,15 @@ template <int D, bool F16, bool kDrop, bool kPlan>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, FwdArgs a) {
-  // Persistent at d = 64 (shared memory has room for a second Q buffer): one CTA per SM runs unit
-  // after unit, so the next unit's Q, K and V copies and its first products overlap the current
+  // Persistent (the balanced block-sparse forward at d = 64, where shared memory has room for a
+  // second Q buffer; pmode 1): one CTA per SM runs unit after unit, claimed in plan order from a
+  // counter by the producer warp and handed to the other roles through two entries in shared
+  // memory, so the next unit's Q, K and V copies and its first products overlap the current
   // unit's last tiles and epilogue; ring positions and barrier phases count across units.
-  //   pmode 1 (the balanced block-sparse forward): units claimed in plan order from a counter by
-  //           the producer warp and handed to the other roles through two entries in shared memory;
-  //   pmode 2 (no mask, packing or split-KV): a fixed sequence of units per CTA, dealt in snake
-  //           order (b, 2G-1-b, 2G+b, ...) so that the heaviest-first order evens out;
-  //   pmode 0: one CTA runs one unit, blockIdx.x.
-  constexpr bool kPersist = D == 64 && !kDrop;
+  // Otherwise (pmode 0) one CTA runs one unit, blockIdx.x.
+  constexpr bool kPersist = kPlan && D == 64 && !kDrop;
   using C = Cfg<D, F16, kPersist>;
-  const int pmode = !kPersist ? 0 : kPlan ? 1 : a.persist_static ? 2 : 0;
+  const int pmode = kPersist ? 1 : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOff);
@@ -169,13 +167,6 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     return reinterpret_cast<UnitEntry*>(smem + C::kBarOff + kBarBytes + e * ent_bytes);
   };
   auto entry_bits = [&](int e) { return reinterpret_cast<uint32_t*>(smem + C::kBarOff + kBarBytes + e * ent_bytes + 16); };
-  // pmode 2: this CTA's k-th unit, or kUnitEnd
-  const int n_static = ((a.N + 2 * BM - 1) / (2 * BM)) * BHs;
-  auto static_unit = [&](int k) {
-    const int G = (int)gridDim.x, b = (int)blockIdx.x;
-    const int x = (k & 1) ? (k + 1) * G - 1 - b : k * G + b;
-    return x < n_static ? x : kUnitEnd;
-  };
   // The geometry of unit x (plan entry wk with a plan); with_range: restrict [j0, j_end) to the
   // unit's range of live key tiles (needs the bitmap `bits`)
   auto make_geo = [&](int x, const int4 wk, const uint32_t* bits, bool with_range) {
@@ -392,43 +383,6 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           for (int m = max(0, n - C::kKSlots); m < n; ++m)
             ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[m % C::kKSlots]), (m / C::kKSlots) & 1, lim_ms, a.err);
         }
-      } else if (pmode == 2 && lane == 0) {
-        // ------------------------------- TMA producer (persistent, fixed sequence) -------------
-        int u = 0;                                   // units run
-        int nq = 0;                                  // Q copies issued
-        int n = 0;                                   // K tiles issued
-        bool ok = true;
-        for (int x = static_unit(0); x != kUnitEnd && ok; x = static_unit(++u)) {
-          const Geo g = make_geo(x, work, nullptr, true);
-          const int qb = u & 1;
-          // Q buffer qb is free once every product of the unit before last has completed
-          if (u >= 2) ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_free[qb]), ((u >> 1) - 1) & 1, lim_ms, a.err);
-          if (!ok) break;
-          const uint32_t qbar = ptx::smem_u32(&bars->q_full[qb]);
-          const uint32_t qdst = qb ? sQ1 : sQ;
-          ptx::mbar_arrive_expect_tx(qbar, 2 * C::kTileBytes);
-          for (int t = 0; t < 2; ++t)
-            for (int hh = 0; hh < D / 64; ++hh)
-              ptx::tma_load_3d(qdst + t * C::kTileBytes + hh * BM * 128, &tmQ, qbar, hh * 64, g.row0 + g.q0 + t * BM, g.qs);
-          ++nq;
-          for (int j = g.next(g.j0); j < g.j_end && ok; j = g.next(j + 1), ++n) {
-            const int slot = n % C::kKSlots;
-            ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[slot]), ((n / C::kKSlots) & 1) ^ 1, lim_ms, a.err);
-            if (!ok) break;
-            if (a.dbg.inject == 1 && n == 0) continue;    // test hook: never deliver this tile
-            const uint32_t fb = ptx::smem_u32(&bars->kv_full[slot]);
-            ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
-            for (int hh = 0; hh < D / 64; ++hh)
-              ptx::tma_load_3d(sKV + slot * C::kTileBytes + hh * BN * 128, &tmK, fb, hh * 64, g.row0 + j * BN, g.ks);
-          }
-        }
-        // Drain: every copy this thread issued must have landed before shared memory is released.
-        for (int m = max(0, nq - 2); m < nq; ++m)
-          ptx::mbar_wait(ptx::smem_u32(&bars->q_full[m & 1]), (m >> 1) & 1, lim_ms, a.err);
-        for (int m = max(0, n - C::kKSlots); m < n; ++m) {
-          if (a.dbg.inject == 1 && m == 0) continue;
-          ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[m % C::kKSlots]), (m / C::kKSlots) & 1, lim_ms, a.err);
-        }
       } else if (pmode == 0 && lane == 0) {
         // ------------------------------- TMA producer -------------------------------------------
         // (Q was requested during the set-up)
@@ -474,10 +428,6 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           if (x == kUnitEnd) break;
           wk = a.plan[x / BHs];
           bits = entry_bits(e);
-        } else if (pmode == 2) {
-          x = static_unit(u);
-          if (x == kUnitEnd) break;
-          bits = nullptr;
         }
         const Geo g = make_geo(x, wk, bits, true);
         for (int j = g.next(g.j0); j < g.j_end && ok; j = g.next(j + 1), ++n) {
@@ -513,10 +463,6 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           if (x == kUnitEnd) break;
           wk = a.plan[x / BHs];
           bits = entry_bits(e);
-        } else if (pmode == 2) {
-          x = static_unit(u);
-          if (x == kUnitEnd) break;
-          bits = nullptr;
         }
         const Geo g = make_geo(x, wk, bits, true);
         const int qb = pmode != 0 ? (u & 1) : 0;
@@ -627,10 +573,6 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (x == kUnitEnd) break;
         wk = a.plan[x / BHs];
         bits = entry_bits(e);
-      } else if (pmode == 2) {
-        x = static_unit(u);
-        if (x == kUnitEnd) break;
-        bits = nullptr;
       }
       const Geo g = make_geo(x, wk, bits, true);
       const int i = g.q0 + t * BM + r;              // query row in the head
@@ -912,17 +854,12 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   if ((e = make_map(&mk, a.k, D, packed ? a.rows : a.Nk, kv_slices, F16)) != cudaSuccess) return e;
   if ((e = make_map(&mv, a.v, D, packed ? a.rows : a.Nk, kv_slices, F16)) != cudaSuccess) return e;
   auto kern = fwd_sm103_kernel<D, F16, kDrop, kPlan>;
-  // d = 64: persistent CTAs (the kernel's pmode 1 with a plan, 2 without a mask, packing or
-  // split-KV), with a second Q buffer; otherwise one CTA per unit
-  constexpr bool kPersist = D == 64 && !kDrop;
-  FwdArgs b = a;
-  b.persist_static = (kPersist && !kPlan && a.block_mask == nullptr && a.cu_seqlens == nullptr && a.n_splits == 1) ? 1 : 0;
-  const bool persistent = kPersist && (kPlan || b.persist_static != 0);
-  if (kPersist && kPlan && (a.next_unit == nullptr || a.pair_bits == nullptr)) return cudaErrorInvalidValue;
+  // the balanced block-sparse forward at d = 64: persistent CTAs (one per SM), a second Q buffer
+  constexpr bool kPersist = kPlan && D == 64 && !kDrop;
+  if (kPersist && (a.next_unit == nullptr || a.pair_bits == nullptr)) return cudaErrorInvalidValue;
   // + the live-tile bitmap of a block-sparse mask (one bit per key tile), or the two unit entries
-  const int smem = (kPersist ? Cfg<D, F16, true>::kSmem : Cfg<D, F16>::kSmem) +
-                   (kPersist && kPlan ? 2 * UnitEntry::bytes(a.bit_words)
-                                      : a.block_mask != nullptr ? ((a.n_tiles + 127) / 128) * 16 : 0);
+  const int smem = kPersist ? Cfg<D, F16, true>::kSmem + 2 * UnitEntry::bytes(a.bit_words)
+                            : Cfg<D, F16>::kSmem + (a.block_mask != nullptr ? ((a.n_tiles + 127) / 128) * 16 : 0);
   // The warp groups re-split the CTA's registers (4 warps down to 88, 8 warps up to 200 per
   // thread); that only completes if the launch holds at least that many registers.
   static LaunchSetup setup;
@@ -930,14 +867,13 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   if ((e = prepare_launch(setup, kern, smem, &regs)) != cudaSuccess) return e;
   if (regs * kThreads < 128 * 88 + 256 * 200) return cudaErrorInvalidConfiguration;
   int units = kPlan ? a.plan_entries * a.B * a.H : ((a.N + 2 * BM - 1) / (2 * BM)) * a.B * a.H * a.n_splits;
-  if (persistent) {                                // one CTA per SM
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if (kPersist) {                                  // one CTA per SM
+    int sms = 0;
+    if ((e = sm_count(&sms)) != cudaSuccess) return e;
     units = min(units, max(1, sms));
   }
   dim3 grid(units);
-  kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, b);
+  kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }
 

@@ -76,9 +76,6 @@ struct FwdArgs {
   int* next_unit;
   const uint32_t* pair_bits;
   int bit_words;
-  // Persistent forward without a plan (d = 64, no mask, no packing, no split-KV): one CTA per SM
-  // runs a fixed sequence of units (set by the launcher).
-  int persist_static;
 };
 
 // The work plan of the balanced block-sparse forward (see FwdArgs::plan).

@@ -48,6 +48,22 @@ struct LaunchSetup {
   std::atomic<int> regs[kDevices] = {};
 };
 
+// The current device's SM count, asked of the runtime once per device (a persistent grid's size).
+inline cudaError_t sm_count(int* out) {
+  static std::atomic<int> cache[LaunchSetup::kDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < LaunchSetup::kDevices;
+  int n = cached ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (n == 0) {
+    if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (cached) cache[dev].store(n, std::memory_order_relaxed);
+  }
+  *out = n;
+  return cudaSuccess;
+}
+
 template <typename Kern>
 cudaError_t prepare_launch(LaunchSetup& c, Kern kern, int smem, int* regs = nullptr) {
   int dev = 0;
