@@ -657,6 +657,11 @@ cudaError_t launch_fwd_sm103(const FwdArgs& a, fa_dtype dt, cudaStream_t s) {
     if (a.d == 64) return launch_fwd_bs_persist_sm103(a, dt, s);
     return dt == FA_FP16 ? launch<128, true, false, true>(a, s) : launch<128, false, false, true>(a, s);
   }
+  // d = 64 without a tile mask, packing or split-KV: the two-CTAs-per-SM kernel of
+  // fa_fwd_bn64_sm103.cu (64-key tiles), faster than this one at every length measured.
+  if (a.d == 64 && a.block_mask == nullptr && a.cu_seqlens == nullptr && a.n_splits == 1 &&
+      a.o_part == nullptr && a.Nk == a.N)
+    return launch_fwd_bn64_sm103(a, dt, s);
   if (dt == FA_FP16) return a.d == 64 ? launch<64, true, false, false>(a, s) : launch<128, true, false, false>(a, s);
   return a.d == 64 ? launch<64, false, false, false>(a, s) : launch<128, false, false, false>(a, s);
 }

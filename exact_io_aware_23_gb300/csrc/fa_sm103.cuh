@@ -15,6 +15,8 @@ namespace fa {
 cudaError_t launch_fwd_sm103(const FwdArgs& a, fa_dtype dt, cudaStream_t s);
 // the balanced block-sparse forward at d = 64 (a plan in `a`): persistent CTAs
 cudaError_t launch_fwd_bs_persist_sm103(const FwdArgs& a, fa_dtype dt, cudaStream_t s);
+// d = 64 without a tile mask, packing, split-KV or dropout: 64-key tiles, two CTAs per SM
+cudaError_t launch_fwd_bn64_sm103(const FwdArgs& a, fa_dtype dt, cudaStream_t s);
 
 // bf16 / fp16 backward main kernel (tcgen05 + TMA), d in {64, 128}; runs between the
 // preprocess and the dQ conversion kernels.

@@ -103,7 +103,9 @@ def test_keep_threshold_extremes(d):
     o, lse = fa.forward(q, k, v, dropout_p=1.0, seed=seed, offset=offset)
     o0, l0 = fa.forward(q, k, v)
     assert torch.count_nonzero(o) == 0
-    assert torch.equal(lse, l0)                        # the statistic of the undropped scores
+    # the statistic of the undropped scores; the plain forward at d = 64 sums l over 64-key
+    # tiles, the dropout one over 128-key tiles: equal up to fp32 summation order
+    assert torch.allclose(lse, l0, rtol=0.0, atol=1e-5)
     grads = fa.backward(q, k, v, o, lse, do, dropout_p=1.0, seed=seed, offset=offset)
     assert fa.check_device_status() == 0
     assert all(torch.count_nonzero(g) == 0 for g in grads)
